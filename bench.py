@@ -1,0 +1,381 @@
+"""Benchmark of the routed MXFP4 MoE layer on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl b300|reference]
+                    [--workload decode1|decode64|prefill4096] [--tokens-per-step M]
+
+Default workload (decode1): one Kimi K3-shaped MoE layer (d=7168, f=1536, E=896, k=16),
+single-token decode, M=1000 seeded tokens per step run back to back as T=1 layer calls.
+A step is one pass of the whole hot path (router, top-k, bucketing, expert FFNs, combine)
+over those tokens.  The 15.7 GB expert pool is far larger than L2, so each token streams
+its 16 experts from HBM (the 25.7 MB router stays L2-resident across tokens, as it would in
+a real decode loop).
+
+Prints one JSON line.  With --gpus N > 1 (launched by torchrun) every rank runs an
+independent replica of the layer (the layer has no cross-GPU step on one node here);
+value = tokens of all ranks / max rank time.
+
+--impl reference times the CPU oracle (plain fp64 C, this repository's oracle/) on the
+host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "MoE-layer tokens/s and MXFP4 weight GB/s as % of B300 HBM peak (T=1/64/4096)"
+D, F, E, K = 7168, 1536, 896, 16
+SEED = 2026
+EXPERT_BYTES = 17_547_264
+GATEUP_BYTES = 11_698_176     # gate + up region of one expert
+DOWN_BYTES = 5_849_088
+ROUTER_BYTES = E * D * 4
+
+WORKLOADS = {
+    "decode1": dict(T=1, desc="K3 MoE layer, single-token decode: d=7168 f=1536 E=896 k=16, T=1 per call"),
+    "decode64": dict(T=64, desc="K3 MoE layer, batched decode: d=7168 f=1536 E=896 k=16, T=64 per call"),
+    "prefill4096": dict(T=4096, desc="K3 MoE layer, prefill: d=7168 f=1536 E=896 k=16, T=4096, +2.0 bias on 32 experts"),
+}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    return ws, rank
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            j = json.load(fh)
+        return j.get("hbm_gbs", 6400.0), j.get("bf16_tflops", 1800.0), "measured"
+    return 6400.0, 1800.0, "fallback"
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        self.proc.wait(timeout=5)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _source_hash(rel: str) -> str:
+    with open(os.path.join(ROOT, rel), "rb") as fh:
+        return hashlib.sha256(fh.read()).hexdigest()[:16]
+
+
+def _traffic_from_profile(kernel_file: str, summary: str):
+    """dram bytes per launch from a committed ncu summary, if it was taken on the current source."""
+    p = os.path.join(ROOT, "profiles", summary)
+    if not os.path.exists(p):
+        return None
+    kv = {}
+    with open(p) as fh:
+        for ln in fh:
+            if ":" in ln and not ln.startswith("#"):
+                a, b = ln.split(":", 1)
+                kv[a.strip()] = b.strip()
+    if kv.get("source_sha256_16") != _source_hash(kernel_file):
+        return None
+    try:
+        return int(float(kv["dram_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+# --------------------------------------------------------------------------- b300 arm ---
+
+def build_layer(torch, k3, T_max, bias=None):
+    import synth
+    nb, sb = synth.expert_bytes(D, F)
+    dn = torch.empty(E * nb, dtype=torch.uint8, device="cuda")
+    ds = torch.empty(E * sb, dtype=torch.uint8, device="cuda")
+    synth.experts_to_device(SEED, 0, 0, E, D, F, dn.data_ptr(), ds.data_ptr())
+    Wr = torch.from_numpy(synth.router_weights(SEED, 0, E, D)).cuda()
+    b = None if bias is None else torch.from_numpy(bias).cuda()
+    layer = k3.k3moe_pack_experts(k3.dims(D, F, E, K, T_max), dn, ds, 1, Wr, b)
+    del dn, ds
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return layer
+
+
+def run_b300(args):
+    import torch
+    import synth
+    import mxfp4_routed_expert_06_b300 as k3
+
+    ws, rank = _dist()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        pg = dist
+    wl = WORKLOADS[args.workload]
+    T = wl["T"]
+    bias = synth.hot_bias(SEED, 0, E, 32, 2.0) if args.workload == "prefill4096" else None
+    layer = build_layer(torch, k3, max(T, 1), bias)
+    calls = args.tokens_per_step if T == 1 else 1
+    tokens_per_step = calls * T
+    # seeded tokens, distinct per rank
+    xs = synth.tokens_bf16(SEED, 0, rank * 10_000_000, tokens_per_step, D)
+    xd = torch.from_numpy(xs.view(np.int16)).cuda()
+    y = torch.empty((tokens_per_step, D), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for c in range(calls):
+            k3.k3moe_layer_forward(layer, xd[c * T:(c + 1) * T], T, y[c * T:(c + 1) * T], stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    def timed(n_steps):
+        if pg:
+            pg.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+        return e0.elapsed_time(e1)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    k3.k3moe_profile(layer, True)
+    ms = timed(args.steps)
+    prof = k3.k3moe_profile_read(layer)
+    k3.k3moe_profile(layer, False)
+    clk = clocks.stop()
+    if pg:
+        t = torch.tensor([ms], device="cuda")
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    tokens = tokens_per_step * args.steps * ws
+    value = tokens / (ms / 1e3)
+
+    # distinct experts touched (algorithmic weight bytes): counted from the actual routing
+    idx = torch.empty((tokens_per_step, K), dtype=torch.int32, device="cuda")
+    w = torch.empty((tokens_per_step, K), dtype=torch.float32, device="cuda")
+    distinct = 0
+    for c in range(calls):
+        k3.k3moe_router_topk(layer, xd[c * T:(c + 1) * T], T, idx[c * T:(c + 1) * T], w[c * T:(c + 1) * T], stream)
+    torch.cuda.synchronize()
+    idx_h = idx.cpu().numpy()
+    for c in range(calls):
+        distinct += len(np.unique(idx_h[c * T:(c + 1) * T]))
+    weight_bytes_per_step = distinct * EXPERT_BYTES
+
+    hbm_peak, bf16_peak, peak_kind = _peaks()
+    # dominant kernel: gate/up (two thirds of the streamed expert bytes)
+    gu_ms, gu_n = prof["gateup"]
+    gu_bytes_per_launch = (distinct / calls) * GATEUP_BYTES
+    achieved = gu_bytes_per_launch / (gu_ms / gu_n / 1e3) / 1e9 if gu_n else None
+    launches = sum(v[1] for v in prof.values())
+    traffic = _traffic_from_profile("mxfp4_routed_expert_06_b300/csrc/decode_ffn.cu", "gateup_decode_k3_t1.txt")
+
+    # end to end through the public host-buffer entry point
+    xh = torch.from_numpy(xs.view(np.int16)).pin_memory()
+    yh = torch.empty((tokens_per_step, D), dtype=torch.float32).pin_memory()
+    for c in range(min(calls, 20)):
+        k3.k3moe_layer_forward_host(layer, xh[c * T:(c + 1) * T], T, yh[c * T:(c + 1) * T], stream)
+    torch.cuda.synchronize()
+    e2e_steps = max(1, min(args.steps, 3))
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        for c in range(calls):
+            k3.k3moe_layer_forward_host(layer, xh[c * T:(c + 1) * T], T, yh[c * T:(c + 1) * T], stream)
+    e2e_s = time.perf_counter() - t0
+    e2e_val = tokens_per_step * e2e_steps / e2e_s
+    if pg:
+        t = torch.tensor([e2e_val], device="cuda")
+        pg.all_reduce(t, op=pg.ReduceOp.MIN)
+        e2e_val = float(t.item()) * ws
+
+    out = None
+    if rank == 0:
+        cpu = None
+        if ws == 1 and not args.no_cpu_baseline:
+            cpu = cpu_baseline(args, seconds=args.cpu_seconds)
+        out = {
+            "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "mxfp4 weights -> f16 mma, f32 accumulate",
+            "data": "synthetic (seeded splitmix64 experts, N(0,1) bf16 tokens, N(0,1/d) router)",
+            "impl": "b300",
+            "config": {"workload": wl["desc"], "calls_per_step": calls, "tokens_per_step": tokens_per_step,
+                       "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                       "l2": "inputs larger than L2: 15.7 GB expert pool streamed from HBM; router L2-resident"},
+            "weight_gbs": round(weight_bytes_per_step * args.steps * ws / (ms / 1e3) / 1e9, 1),
+            "weight_pct_of_hbm_peak": round(100 * weight_bytes_per_step * args.steps / (ms / 1e3) / 1e9 / hbm_peak, 1),
+            "distinct_experts_per_call": round(distinct / calls, 2),
+            "roofline": {"bound": "hbm", "kernel": "gateup_kernel (gate/up + SwiGLU, register decode)",
+                         "achieved": None if achieved is None else round(achieved, 1),
+                         "peak": hbm_peak, "unit": "GB/s",
+                         "frac": None if achieved is None else round(achieved / hbm_peak, 4),
+                         "peak_kind": f"{peak_kind} (HBM copy peak)",
+                         "algorithmic_bytes_per_launch": int(gu_bytes_per_launch), "traffic": traffic},
+            "kernel_ms_per_launch": {k: round(v[0] / v[1], 5) for k, v in prof.items() if v[1]},
+            "gpu_launches": int(launches),
+            "e2e": {"value": round(e2e_val, 3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": tokens_per_step * D * 2, "d2h_bytes_per_step": tokens_per_step * D * 4},
+            "clocks": clk,
+            "cpu_baseline": cpu,
+        }
+    k3.k3moe_layer_free(layer)
+    if pg:
+        pg.destroy_process_group()
+    return out
+
+
+# ---------------------------------------------------------------------- oracle arm ---
+
+def _oracle_tokens(n_tokens, rank_offset=0):
+    """The oracle on n_tokens single-token calls of the K3 layer: returns seconds and threads used."""
+    import oracle
+    import synth
+    Wr = synth.router_weights(SEED, 0, E, D)
+    xs = synth.tokens_bf16(SEED, 0, rank_offset, n_tokens, D)
+    # expert bytes are regenerated on the host; that is input preparation, not timed
+    t_total = 0.0
+    for t in range(n_tokens):
+        t0 = time.perf_counter()
+        idx, w, _, _ = oracle.router(xs[t:t + 1], Wr, None, K)
+        t_total += time.perf_counter() - t0
+        nibs, scls = [], []
+        for e in idx[0].tolist():
+            n, s = synth.experts(SEED, 0, e, e + 1, D, F)
+            nibs.append(n[0])
+            scls.append(s[0])
+        t0 = time.perf_counter()
+        oracle.moe(xs[t:t + 1], w, nibs, scls, F)
+        t_total += time.perf_counter() - t0
+    return t_total, oracle.max_threads()
+
+
+def cpu_baseline(args, seconds=20.0):
+    """The oracle as it stands, on a bounded sample of the decode workload."""
+    import oracle
+    oracle.build()
+    n = 1
+    sec, cores = _oracle_tokens(n)
+    while sec < seconds * 0.5 and n < 64:
+        n2 = max(1, int(n * seconds / max(sec, 1e-3) * 0.5))
+        s2, _ = _oracle_tokens(n2, 100 + n)
+        n, sec = n2, s2
+    return {"value": round(n / sec, 6), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} single-token K3 layer calls (router over 896 experts + 16 expert FFNs each), "
+                      f"fp64 scalar MXFP4 decode, {sec:.1f} s"}
+
+
+def run_reference(args):
+    ws, rank = _dist()
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    per_step = 1
+    for _ in range(args.warmup):
+        _oracle_tokens(per_step, 500)
+    total = 0.0
+    cores = 1
+    for s in range(args.steps):
+        sec, cores = _oracle_tokens(per_step, 1000 + s)
+        total += sec
+    value = per_step * args.steps / total
+    wl = WORKLOADS["decode1"]
+    return {
+        "metric": METRIC, "value": round(value, 6), "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (same generator as the b300 arm)",
+        "impl": "reference",
+        "config": {"workload": wl["desc"], "calls_per_step": per_step, "tokens_per_step": per_step,
+                   "parallelism": "host cores (OpenMP)"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{per_step} single-token layer call per step (bounded sample of the "
+                                   f"1000-token decode workload)"},
+        "e2e": {"value": round(value, 6), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="b300", choices=["b300", "reference"])
+    ap.add_argument("--workload", default="decode1", choices=sorted(WORKLOADS))
+    ap.add_argument("--tokens-per-step", type=int, default=1000)
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    out = run_reference(args) if args.impl == "reference" else run_b300(args)
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,197 @@
+/*
+ * k3moe.h -- C ABI of the routed mixture-of-experts layer on MXFP4 experts (B300, sm_103a).
+ *
+ * The layer (pages on the kimi-k3-in-c engine, fiv.co.kr "kimi-k3-in-c deep dive"):
+ *   router      sigmoid scores of x against W_r; a per-expert bias steers the selection
+ *               only; the top-k experts (16 of 896 in Kimi K3) are mixed with weights taken
+ *               from the unbiased scores, renormalised to sum 1
+ *               (section "what you learn", router paragraph; invariants table, row 5;
+ *               glossary entry MoE)
+ *   experts     every expert is a SwiGLU FFN whose gate/up/down weights stay MXFP4 -- E2M1
+ *               nibbles with one E8M0 scale per 32 values, value = E2M1[nibble]*2^(scale-127)
+ *               -- and are multiplied without being expanded to a dense copy
+ *               (section "four reductions", reduction 1; glossary entry MXFP4)
+ *   combine     y[t] = sum over the k slots, in slot order, of w[t,slot] * expert_out
+ *   cache       an LRU expert cache whose size changes speed, never the output
+ *               (section "four reductions", expert LRU paragraph; opening: "the output is
+ *               byte-identical whatever the memory budget")
+ *
+ * Conventions for every call:
+ *   - Return 0 on success or a negative K3MOE_ERR_* code; k3moe_last_error() then gives a
+ *     message (thread-local, valid until the next failing call on the same thread).
+ *   - Arguments are checked before any device work is queued; a failed check changes nothing.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Device
+ *     work is queued on it asynchronously unless a call says otherwise.
+ *   - "device pointer" means memory of the current CUDA device, allocated by the caller (for
+ *     example by PyTorch); the library never frees caller memory.  The library owns what it
+ *     allocates: packed weights, workspace, cache slots, pinned pools.
+ *   - One layer object must not be used from two streams at the same time: calls share its
+ *     workspace.  Different layer objects are independent (a shared cache excepted).
+ *   - Canonical MXFP4 input layout, per expert e (experts back to back):
+ *       nibbles  [3][rows][cols/2] bytes: matrix 0 = gate W_g [f][d], 1 = up W_u [f][d],
+ *                2 = down W_d [d][f]; element 2i of a row in the LOW nibble of byte i;
+ *                E2M1 codes per OCP MX v1.0 (bit 3 sign, bits 2..1 exponent, bit 0 mantissa)
+ *       scales   [3][rows][cols/32] E8M0 bytes; block b of a row covers columns 32b..32b+31
+ *     so one expert is 3*f*d/2 nibble bytes + 3*f*d/32 scale bytes (17,547,264 bytes in total
+ *     at d=7168, f=1536, the count printed in "four reductions", reduction 1).
+ */
+#ifndef K3MOE_H
+#define K3MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define K3MOE_OK 0
+#define K3MOE_ERR_INVALID_ARG (-1)      /* bad pointer, size, dimension or option */
+#define K3MOE_ERR_OOM (-2)              /* device or pinned host allocation failed */
+#define K3MOE_ERR_CUDA (-3)             /* a CUDA runtime call or kernel launch failed */
+#define K3MOE_ERR_TIMEOUT (-4)          /* a bounded device-side wait gave up */
+#define K3MOE_ERR_BUDGET_TOO_SMALL (-5) /* the cache cannot hold the experts one call needs */
+#define K3MOE_ERR_UNSUPPORTED (-6)      /* valid request this build does not implement */
+
+/* Layer dimensions, validated strictly (unknown or inconsistent values are refused, never
+ * defaulted -- the engine's strict config loading, "what you learn", last paragraph):
+ *   d      model width, multiple of 128, <= 16384
+ *   f      expert intermediate width, multiple of 128, <= 16384
+ *   E      number of routed experts, 1..4096
+ *   k      experts per token, 1..min(E, 32)
+ *   T_max  largest token count a call may pass, 1..65536 (sizes the workspace) */
+typedef struct {
+  int d, f, E, k, T_max;
+} k3moe_dims;
+
+typedef struct k3moe_layer k3moe_layer; /* opaque: packed weights, router, workspace */
+typedef struct k3moe_cache k3moe_cache; /* opaque: device expert slots + LRU state */
+
+typedef struct {
+  uint64_t hits;       /* experts found resident */
+  uint64_t misses;     /* experts copied from the pinned pool */
+  uint64_t evictions;  /* resident experts replaced */
+  uint64_t h2d_bytes;  /* bytes copied host -> device by misses */
+  double h2d_ms;       /* device time of those copies (CUDA events on the copy stream) */
+  uint64_t calls;      /* layer calls served */
+} k3moe_cache_stats_t;
+
+/* Bytes of one expert in the packed device layout (equal to the canonical byte count:
+ * 3*f*d/2 + 3*f*d/32).  Returns 0 for invalid dims. */
+size_t k3moe_packed_expert_bytes(const k3moe_dims* dims);
+
+/* Build a layer: repack all E experts from the canonical layout into the library's packed
+ * layout (16-row x 128-column tiles, nibbles in tensor-core fragment order with each tile's
+ * scales stored right after it; lossless), and copy the router.
+ *   dims          layer dimensions (see k3moe_dims)
+ *   canon_nib     E * 3*f*d/2 bytes, canonical nibbles of experts 0..E-1
+ *   canon_scale   E * 3*f*d/32 bytes, canonical E8M0 scales; a scale byte of 255 (NaN) is
+ *                 refused with K3MOE_ERR_INVALID_ARG (checked on the device, reported here)
+ *   src_on_device 1: canon_nib, canon_scale, W_r and bias are device pointers; 0: host
+ *   W_r           router weights [E][d] float32, row-major
+ *   bias          selection bias [E] float32, or NULL for all zeros
+ *   cache         NULL: packed experts live in device memory owned by the layer.
+ *                 non-NULL: they live in a pinned host pool owned by the layer, and are
+ *                 brought to the device through `cache` (which may serve several layers)
+ *   stream        stream for the copies and the pack kernel; the call synchronises it
+ *                 before returning (the source buffers may be freed afterwards)
+ *   out           receives the new layer; free it with k3moe_layer_free
+ * Errors: INVALID_ARG (dims, NULL pointers, NaN scale), OOM, CUDA. */
+int k3moe_pack_experts(const k3moe_dims* dims, const void* canon_nib, const void* canon_scale, int src_on_device,
+                       const float* W_r, const float* bias, k3moe_cache* cache, void* stream, k3moe_layer** out);
+
+/* Router alone ("what you learn", router paragraph; invariants row 5):
+ *   logit[t,e] = sum_j x[t,j]*W_r[e,j] (fp32 accumulate), sigma = 1/(1+exp(-logit)),
+ *   key = sigma + bias[e]; idx[t,:] = the k experts with the largest keys in descending key
+ *   order, ties to the lower expert id; w[t,i] = sigma[idx[t,i]] / sum_i sigma[idx[t,i]].
+ *   x    device pointer, [T][d] bf16, row-major
+ *   T    1..T_max
+ *   idx  device pointer, [T][k] int32 (output)
+ *   w    device pointer, [T][k] float32 (output)
+ * Errors: INVALID_ARG, CUDA. */
+int k3moe_router_topk(k3moe_layer* layer, const void* x_bf16, int T, int32_t* idx, float* w, void* stream);
+
+/* Token-to-expert bucketing of T*k picks (pick p = t*k + slot):
+ *   counts[e]  number of picks routed to expert e                      [E] int32
+ *   offsets    exclusive prefix sum of counts in expert-id order       [E+1] int32
+ *   perm       for each expert in id order, its picks in ascending p   [T*k] int32
+ * Deterministic (a pure function of idx).  All pointers are device pointers.
+ *   idx  [T][k] int32 expert ids, each in 0..E-1 (ids out of range: the pick is dropped from
+ *        every expert and perm's tail is left unspecified; no memory outside the outputs is
+ *        touched).
+ * Errors: INVALID_ARG, CUDA. */
+int k3moe_bucket(k3moe_layer* layer, const int32_t* idx, int T, int32_t* counts, int32_t* offsets, int32_t* perm,
+                 void* stream);
+
+/* The whole layer: router -> top-k -> bucketing -> per-expert SwiGLU FFN on the MXFP4
+ * weights -> combine ("four reductions", reduction 1; invariants row 5):
+ *   y[t,:] = sum_{slot=0..k-1} w[t,slot] * W_d,e (silu(W_g,e x_t) * (W_u,e x_t)),
+ *   e = idx[t,slot], silu(z) = z/(1+exp(-z)), summed in slot order.
+ *   x  device pointer, [T][d] bf16 row-major;  y  device pointer, [T][d] float32 (output).
+ *   T  1..T_max.  y excludes any residual.
+ * The result does not depend on the cache budget, on which experts were resident, or on
+ * the run (bitwise).  Small T runs the register-decode path, large T the tcgen05 grouped
+ * GEMM path (k3moe_set_option); the two agree within the accuracy bound, not bitwise.
+ * In cache mode the call synchronises `stream` once (to learn which experts it needs).
+ * Errors: INVALID_ARG, CUDA, TIMEOUT, BUDGET_TOO_SMALL, OOM (cache mode). */
+int k3moe_layer_forward(k3moe_layer* layer, const void* x_bf16, int T, float* y, void* stream);
+
+/* k3moe_layer_forward with HOST buffers: copies x (host, [T][d] bf16) to the device, runs
+ * the layer, copies y back to host ([T][d] float32) and synchronises `stream`.  Pinned host
+ * memory gives the fastest copies; pageable memory also works.  Errors as layer_forward. */
+int k3moe_layer_forward_host(k3moe_layer* layer, const void* x_bf16_host, int T, float* y_host, void* stream);
+
+/* Options. */
+#define K3MOE_OPT_PATH 1        /* value: K3MOE_PATH_AUTO (default), _DECODE, _GEMM */
+#define K3MOE_OPT_GEMM_MIN_T 2  /* value: smallest T the AUTO path sends to the grouped GEMM */
+#define K3MOE_PATH_AUTO 0
+#define K3MOE_PATH_DECODE 1
+#define K3MOE_PATH_GEMM 2
+int k3moe_set_option(k3moe_layer* layer, int option, long long value);
+
+/* Per-kernel device times (CUDA events around each launch, on the launch stream).
+ * k3moe_profile(layer, 1) clears the totals and starts recording; (layer, 0) stops.
+ * k3moe_profile_read synchronises the layer's last stream and fills `out` (K3MOE_K_COUNT
+ * entries). */
+enum {
+  K3MOE_K_ROUTER = 0,   /* router logits (+ fused top-k and bucketing for small T) */
+  K3MOE_K_TOPK = 1,     /* top-k for large T */
+  K3MOE_K_BUCKET = 2,   /* bucketing for large T */
+  K3MOE_K_GATEUP = 3,   /* gate/up + SwiGLU, register-decode path */
+  K3MOE_K_DOWN = 4,     /* down projection + combine, register-decode path */
+  K3MOE_K_GEMM_GU = 5,  /* gate/up + SwiGLU, tcgen05 grouped GEMM */
+  K3MOE_K_GEMM_DN = 6,  /* down projection, tcgen05 grouped GEMM */
+  K3MOE_K_COMBINE = 7,  /* slot-ordered combine for the GEMM path */
+  K3MOE_K_GATHER = 8,   /* activation gather for the GEMM path */
+  K3MOE_K_COUNT = 9
+};
+typedef struct {
+  double ms_total;
+  long long launches;
+} k3moe_kernel_time;
+int k3moe_profile(k3moe_layer* layer, int enable);
+int k3moe_profile_read(k3moe_layer* layer, k3moe_kernel_time* out);
+
+/* Copy expert e's packed bytes (k3moe_packed_expert_bytes) to host memory `dst`;
+ * synchronous.  For layout checks. */
+int k3moe_read_packed(k3moe_layer* layer, int e, void* dst);
+
+void k3moe_layer_free(k3moe_layer* layer);
+
+/* Expert cache ("four reductions", expert LRU paragraph).  budget_bytes of device memory
+ * are split into floor(budget/slot_bytes) slots, each holding one packed expert;
+ * slot_bytes must equal k3moe_packed_expert_bytes of the layers that use the cache.
+ * Least-recently-used experts are replaced; misses are copied from the layer's pinned pool
+ * on a side stream.  Errors: INVALID_ARG (budget < one slot), OOM, CUDA. */
+int k3moe_cache_create(size_t budget_bytes, size_t slot_bytes, k3moe_cache** out);
+int k3moe_cache_stats(const k3moe_cache* cache, k3moe_cache_stats_t* out);
+int k3moe_cache_reset_stats(k3moe_cache* cache);
+/* Destroy after every layer that uses it has been freed. */
+void k3moe_cache_destroy(k3moe_cache* cache);
+
+const char* k3moe_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,618 @@
+// capi.cu -- the C ABI (include/k3moe.h): argument checks, ownership, workspace, dispatch,
+// and the expert cache's host-side LRU bookkeeping.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <list>
+#include <unordered_map>
+#include <utility>
+#include <vector>
+
+#include "k3moe_internal.cuh"
+
+using namespace k3;
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+#define CUDA_TRY(call)                                                                   \
+  do {                                                                                   \
+    cudaError_t e_ = (call);                                                             \
+    if (e_ != cudaSuccess) return fail(K3MOE_ERR_CUDA, "%s: %s", #call, cudaGetErrorString(e_)); \
+  } while (0)
+
+int check_dims(const k3moe_dims* d) {
+  if (!d) return fail(K3MOE_ERR_INVALID_ARG, "dims is NULL");
+  if (d->d <= 0 || d->d % 128 != 0 || d->d > 16384)
+    return fail(K3MOE_ERR_INVALID_ARG, "d=%d must be a positive multiple of 128, <= 16384", d->d);
+  if (d->f <= 0 || d->f % 128 != 0 || d->f > 16384)
+    return fail(K3MOE_ERR_INVALID_ARG, "f=%d must be a positive multiple of 128, <= 16384", d->f);
+  if (d->E < 1 || d->E > 4096) return fail(K3MOE_ERR_INVALID_ARG, "E=%d must be in 1..4096", d->E);
+  if (d->k < 1 || d->k > d->E || d->k > 32)
+    return fail(K3MOE_ERR_INVALID_ARG, "k=%d must be in 1..min(E, 32)", d->k);
+  if (d->T_max < 1 || d->T_max > 65536) return fail(K3MOE_ERR_INVALID_ARG, "T_max=%d must be in 1..65536", d->T_max);
+  return K3MOE_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Copy raw bytes into the device (from host or device memory).
+cudaError_t to_device(void* dst, const void* src, size_t n, int src_on_device, cudaStream_t s) {
+  return cudaMemcpyAsync(dst, src, n, src_on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, s);
+}
+
+struct TimedLaunch {
+  int kid;
+  cudaEvent_t a, b;
+};
+
+}  // namespace
+
+struct k3moe_cache {
+  size_t slot_bytes = 0;
+  int n_slots = 0;
+  uint8_t* slots = nullptr;
+  cudaStream_t copy_stream = nullptr;
+  std::list<int> lru;  // front = most recently used slot
+  std::vector<std::list<int>::iterator> lru_pos;
+  std::vector<long long> slot_key;  // (layer uid << 32) | expert, or -1 when empty
+  std::unordered_map<long long, int> where;
+  k3moe_cache_stats_t st{};
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> pending;  // copy timings not yet read
+  std::vector<cudaEvent_t> free_events;
+  int users = 0;
+  int next_uid = 1;
+};
+
+struct k3moe_layer {
+  k3moe_dims dims{};
+  size_t exp_bytes = 0;
+  uint8_t* packed = nullptr;    // device, E * exp_bytes (device mode)
+  uint8_t* pool = nullptr;      // pinned host, E * exp_bytes (cache mode)
+  float* Wr = nullptr;          // device [E][d]
+  float* bias = nullptr;        // device [E] or nullptr
+  const uint8_t** eptr_dev = nullptr;  // device [E]
+  const uint8_t** eptr_host = nullptr; // pinned host [E] (cache mode staging)
+  int32_t* act_host = nullptr;         // pinned host [E+1] (cache mode)
+  void* ws_block = nullptr;
+  Workspace ws;
+  k3moe_cache* cache = nullptr;
+  int uid = 0;
+  int path = K3MOE_PATH_AUTO;
+  long long gemm_min_t = 1LL << 40;
+  bool profiling = false;
+  std::vector<TimedLaunch> timed;
+  std::vector<cudaEvent_t> spare_events;
+  double prof_ms[K3MOE_K_COUNT] = {};
+  long long prof_n[K3MOE_K_COUNT] = {};
+  cudaStream_t last_stream = nullptr;
+  cudaEvent_t copies_done = nullptr;
+  uint16_t* x_stage = nullptr;  // forward_host staging
+  float* y_stage = nullptr;
+};
+
+namespace {
+
+cudaEvent_t take_event(k3moe_layer* L) {
+  if (!L->spare_events.empty()) {
+    cudaEvent_t e = L->spare_events.back();
+    L->spare_events.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Launch helper: optional event pair around the launch, on the launch stream.
+template <typename F>
+int timed_launch(k3moe_layer* L, int kid, cudaStream_t s, F&& launch) {
+  TimedLaunch tl{kid, nullptr, nullptr};
+  if (L->profiling) {
+    tl.a = take_event(L);
+    tl.b = take_event(L);
+    cudaEventRecord(tl.a, s);
+  }
+  cudaError_t e = launch();
+  if (e != cudaSuccess) return fail(K3MOE_ERR_CUDA, "kernel %d launch: %s", kid, cudaGetErrorString(e));
+  if (L->profiling) {
+    cudaEventRecord(tl.b, s);
+    L->timed.push_back(tl);
+  }
+  return K3MOE_OK;
+}
+
+int alloc_workspace(k3moe_layer* L) {
+  const k3moe_dims& D = L->dims;
+  const size_t T = D.T_max, P = (size_t)D.T_max * D.k;
+  struct Item {
+    void** dst;
+    size_t bytes;
+  };
+  Workspace& w = L->ws;
+  std::vector<Item> items = {
+      {(void**)&w.logits, T * D.E * 4},  {(void**)&w.xfrag, T * D.d * 2},       {(void**)&w.xscale, T * 4},
+      {(void**)&w.idx, P * 4},           {(void**)&w.w, P * 4},                 {(void**)&w.counts, (size_t)D.E * 4},
+      {(void**)&w.offsets, (size_t)(D.E + 1) * 4}, {(void**)&w.perm, P * 4},    {(void**)&w.act, (size_t)D.E * 4},
+      {(void**)&w.nact, 4},              {(void**)&w.hfrag, P * D.f * 2},       {(void**)&w.hscale, P * (D.f / 32) * 4},
+      {(void**)&w.obuf, P * D.d * 4},    {(void**)&w.arrive, T * (D.d / 64) * 4}, {(void**)&w.sync, 64},
+      {(void**)&w.bad, 4},
+  };
+  size_t total = 0;
+  for (auto& it : items) total += align256(it.bytes);
+  if (cudaMalloc(&L->ws_block, total) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(K3MOE_ERR_OOM, "workspace: cudaMalloc(%zu) failed", total);
+  }
+  size_t off = 0;
+  for (auto& it : items) {
+    *it.dst = (char*)L->ws_block + off;
+    off += align256(it.bytes);
+  }
+  CUDA_TRY(cudaMemset(L->ws_block, 0, total));
+  return K3MOE_OK;
+}
+
+void free_layer(k3moe_layer* L) {
+  if (!L) return;
+  if (L->last_stream) cudaStreamSynchronize(L->last_stream);
+  cudaFree(L->packed);
+  cudaFreeHost(L->pool);
+  cudaFree(L->Wr);
+  cudaFree(L->bias);
+  cudaFree((void*)L->eptr_dev);
+  cudaFreeHost((void*)L->eptr_host);
+  cudaFreeHost(L->act_host);
+  cudaFree(L->ws_block);
+  cudaFree(L->x_stage);
+  cudaFree(L->y_stage);
+  for (auto& t : L->timed) {
+    cudaEventDestroy(t.a);
+    cudaEventDestroy(t.b);
+  }
+  for (auto e : L->spare_events) cudaEventDestroy(e);
+  if (L->copies_done) cudaEventDestroy(L->copies_done);
+  if (L->cache) {
+    // drop this layer's experts from the cache
+    k3moe_cache* C = L->cache;
+    for (int s = 0; s < C->n_slots; ++s) {
+      if (C->slot_key[s] >= 0 && (int)(C->slot_key[s] >> 32) == L->uid) {
+        C->where.erase(C->slot_key[s]);
+        C->slot_key[s] = -1;
+      }
+    }
+    C->users -= 1;
+  }
+  delete L;
+}
+
+bool use_gemm(const k3moe_layer* L, int T) {
+  if (L->path == K3MOE_PATH_GEMM) return true;
+  if (L->path == K3MOE_PATH_DECODE) return false;
+  return (long long)T >= L->gemm_min_t;
+}
+
+// Router + selection + bucketing into the workspace.
+int run_routing(k3moe_layer* L, const void* x, int T, cudaStream_t s) {
+  const k3moe_dims& D = L->dims;
+  RouterArgs ra{reinterpret_cast<const uint16_t*>(x), L->Wr, L->bias, T, D.d, D.E, D.k, L->ws, 0};
+  ra.fuse_select = (T * D.k <= 1024) ? 1 : 0;
+  int rc = timed_launch(L, KID_ROUTER, s, [&] { return launch_router(ra, s); });
+  if (rc) return rc;
+  if (!ra.fuse_select) {
+    rc = timed_launch(L, KID_TOPK, s,
+                      [&] { return launch_topk(L->ws.logits, L->bias, T, D.E, D.k, L->ws.idx, L->ws.w, s); });
+    if (rc) return rc;
+    rc = timed_launch(L, KID_BUCKET, s, [&] {
+      return launch_bucket(L->ws.idx, T, D.k, D.E, L->ws.counts, L->ws.offsets, L->ws.perm, L->ws.act, L->ws.nact,
+                           s);
+    });
+    if (rc) return rc;
+  }
+  return K3MOE_OK;
+}
+
+// Cache mode: make every active expert resident; fill eptr_dev for them.
+int make_resident(k3moe_layer* L, cudaStream_t s) {
+  k3moe_cache* C = L->cache;
+  const int E = L->dims.E;
+  CUDA_TRY(cudaMemcpyAsync(L->act_host, L->ws.nact, 4, cudaMemcpyDeviceToHost, s));
+  CUDA_TRY(cudaMemcpyAsync(L->act_host + 1, L->ws.act, (size_t)E * 4, cudaMemcpyDeviceToHost, s));
+  CUDA_TRY(cudaStreamSynchronize(s));
+  const int nact = L->act_host[0];
+  if (nact < 0 || nact > E) return fail(K3MOE_ERR_CUDA, "corrupt active-expert count %d", nact);
+  if (nact > C->n_slots)
+    return fail(K3MOE_ERR_BUDGET_TOO_SMALL, "call needs %d experts resident, cache has %d slots", nact, C->n_slots);
+  const int32_t* act = L->act_host + 1;
+  // pass 1: hits are touched first so that no expert of this call is evicted
+  std::vector<int> miss;
+  for (int i = 0; i < nact; ++i) {
+    const long long key = ((long long)L->uid << 32) | act[i];
+    auto it = C->where.find(key);
+    if (it != C->where.end()) {
+      const int slot = it->second;
+      C->lru.erase(C->lru_pos[slot]);
+      C->lru.push_front(slot);
+      C->lru_pos[slot] = C->lru.begin();
+      L->eptr_host[act[i]] = C->slots + (size_t)slot * C->slot_bytes;
+      C->st.hits += 1;
+    } else {
+      miss.push_back(act[i]);
+    }
+  }
+  if (!miss.empty()) {
+    cudaEvent_t a, b;
+    if (!C->free_events.empty()) { a = C->free_events.back(); C->free_events.pop_back(); } else cudaEventCreate(&a);
+    if (!C->free_events.empty()) { b = C->free_events.back(); C->free_events.pop_back(); } else cudaEventCreate(&b);
+    // the copy stream must not overwrite a slot that earlier queued work on `s` may still read
+    CUDA_TRY(cudaEventRecord(L->copies_done, s));
+    CUDA_TRY(cudaStreamWaitEvent(C->copy_stream, L->copies_done, 0));
+    CUDA_TRY(cudaEventRecord(a, C->copy_stream));
+    for (int e : miss) {
+      const int slot = C->lru.back();  // least recently used; never one touched in pass 1
+      C->lru.pop_back();
+      if (C->slot_key[slot] >= 0) {
+        C->where.erase(C->slot_key[slot]);
+        C->st.evictions += 1;
+      }
+      const long long key = ((long long)L->uid << 32) | e;
+      C->slot_key[slot] = key;
+      C->where[key] = slot;
+      C->lru.push_front(slot);
+      C->lru_pos[slot] = C->lru.begin();
+      uint8_t* dst = C->slots + (size_t)slot * C->slot_bytes;
+      CUDA_TRY(cudaMemcpyAsync(dst, L->pool + (size_t)e * L->exp_bytes, L->exp_bytes, cudaMemcpyHostToDevice,
+                               C->copy_stream));
+      L->eptr_host[e] = dst;
+      C->st.misses += 1;
+      C->st.h2d_bytes += L->exp_bytes;
+    }
+    CUDA_TRY(cudaEventRecord(b, C->copy_stream));
+    C->pending.emplace_back(a, b);
+    CUDA_TRY(cudaStreamWaitEvent(s, b, 0));
+  }
+  C->st.calls += 1;
+  CUDA_TRY(cudaMemcpyAsync((void*)L->eptr_dev, L->eptr_host, (size_t)E * sizeof(void*), cudaMemcpyHostToDevice, s));
+  return K3MOE_OK;
+}
+
+int forward_impl(k3moe_layer* L, const void* x, int T, float* y, cudaStream_t s) {
+  const k3moe_dims& D = L->dims;
+  L->last_stream = s;
+  if (use_gemm(L, T)) return fail(K3MOE_ERR_UNSUPPORTED, "grouped-GEMM path is not built yet");
+  int rc = run_routing(L, x, T, s);
+  if (rc) return rc;
+  if (L->cache) {
+    rc = make_resident(L, s);
+    if (rc) return rc;
+  }
+  FfnArgs fa{L->eptr_dev, D.d, D.f, D.E, D.k, T, L->ws, y, std::min(D.E, T * D.k)};
+  rc = timed_launch(L, KID_GATEUP, s, [&] { return launch_gateup(fa, s); });
+  if (rc) return rc;
+  return timed_launch(L, KID_DOWN, s, [&] { return launch_down(fa, s); });
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t k3moe_packed_expert_bytes(const k3moe_dims* dims) {
+  if (check_dims(dims) != K3MOE_OK) return 0;
+  return packed_expert_bytes(dims->d, dims->f);
+}
+
+const char* k3moe_last_error(void) { return g_err.c_str(); }
+
+int k3moe_cache_create(size_t budget_bytes, size_t slot_bytes, k3moe_cache** out) {
+  if (!out) return fail(K3MOE_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (slot_bytes == 0 || slot_bytes % 256 != 0)
+    return fail(K3MOE_ERR_INVALID_ARG, "slot_bytes=%zu must be a positive multiple of 256", slot_bytes);
+  if (budget_bytes < slot_bytes)
+    return fail(K3MOE_ERR_INVALID_ARG, "budget %zu bytes is smaller than one slot (%zu)", budget_bytes, slot_bytes);
+  const size_t n = budget_bytes / slot_bytes;
+  if (n > (1u << 30)) return fail(K3MOE_ERR_INVALID_ARG, "too many slots");
+  k3moe_cache* C = new k3moe_cache();
+  C->slot_bytes = slot_bytes;
+  C->n_slots = (int)n;
+  if (cudaMalloc(&C->slots, n * slot_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    delete C;
+    return fail(K3MOE_ERR_OOM, "cache: cudaMalloc(%zu) failed", n * slot_bytes);
+  }
+  if (cudaStreamCreateWithFlags(&C->copy_stream, cudaStreamNonBlocking) != cudaSuccess) {
+    cudaFree(C->slots);
+    delete C;
+    return fail(K3MOE_ERR_CUDA, "cache: stream creation failed");
+  }
+  C->lru_pos.resize(n);
+  C->slot_key.assign(n, -1);
+  for (int i = 0; i < (int)n; ++i) {
+    C->lru.push_back(i);
+    C->lru_pos[i] = std::prev(C->lru.end());
+  }
+  *out = C;
+  return K3MOE_OK;
+}
+
+int k3moe_cache_stats(const k3moe_cache* cc, k3moe_cache_stats_t* out) {
+  if (!cc || !out) return fail(K3MOE_ERR_INVALID_ARG, "NULL argument");
+  k3moe_cache* C = const_cast<k3moe_cache*>(cc);
+  for (auto& pr : C->pending) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(pr.second) == cudaSuccess && cudaEventElapsedTime(&ms, pr.first, pr.second) == cudaSuccess)
+      C->st.h2d_ms += ms;
+    C->free_events.push_back(pr.first);
+    C->free_events.push_back(pr.second);
+  }
+  C->pending.clear();
+  *out = C->st;
+  return K3MOE_OK;
+}
+
+int k3moe_cache_reset_stats(k3moe_cache* C) {
+  if (!C) return fail(K3MOE_ERR_INVALID_ARG, "cache is NULL");
+  k3moe_cache_stats_t tmp;
+  k3moe_cache_stats(C, &tmp);
+  C->st = k3moe_cache_stats_t{};
+  return K3MOE_OK;
+}
+
+void k3moe_cache_destroy(k3moe_cache* C) {
+  if (!C) return;
+  if (C->copy_stream) {
+    cudaStreamSynchronize(C->copy_stream);
+    cudaStreamDestroy(C->copy_stream);
+  }
+  for (auto& pr : C->pending) {
+    cudaEventDestroy(pr.first);
+    cudaEventDestroy(pr.second);
+  }
+  for (auto e : C->free_events) cudaEventDestroy(e);
+  cudaFree(C->slots);
+  delete C;
+}
+
+int k3moe_pack_experts(const k3moe_dims* dims, const void* canon_nib, const void* canon_scale, int src_on_device,
+                       const float* W_r, const float* bias, k3moe_cache* cache, void* stream, k3moe_layer** out) {
+  if (!out) return fail(K3MOE_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if (!canon_nib || !canon_scale || !W_r) return fail(K3MOE_ERR_INVALID_ARG, "NULL input pointer");
+  if (src_on_device != 0 && src_on_device != 1) return fail(K3MOE_ERR_INVALID_ARG, "src_on_device must be 0 or 1");
+  const k3moe_dims D = *dims;
+  const size_t eb = packed_expert_bytes(D.d, D.f);
+  if (cache && cache->slot_bytes != eb)
+    return fail(K3MOE_ERR_INVALID_ARG, "cache slot_bytes %zu != packed expert bytes %zu", cache->slot_bytes, eb);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  k3moe_layer* L = new k3moe_layer();
+  L->dims = D;
+  L->exp_bytes = eb;
+  L->cache = cache;
+  auto bail = [&](int code) {
+    free_layer(L);
+    return code;
+  };
+  if ((rc = alloc_workspace(L))) return bail(rc);
+  if (cudaEventCreateWithFlags(&L->copies_done, cudaEventDisableTiming) != cudaSuccess)
+    return bail(fail(K3MOE_ERR_CUDA, "event creation failed"));
+  if (cudaMalloc(&L->Wr, (size_t)D.E * D.d * 4) != cudaSuccess ||
+      (bias && cudaMalloc(&L->bias, (size_t)D.E * 4) != cudaSuccess) ||
+      cudaMalloc((void**)&L->eptr_dev, (size_t)D.E * sizeof(void*)) != cudaSuccess) {
+    cudaGetLastError();
+    return bail(fail(K3MOE_ERR_OOM, "router/pointer table allocation failed"));
+  }
+  if (to_device(L->Wr, W_r, (size_t)D.E * D.d * 4, src_on_device, s) != cudaSuccess ||
+      (bias && to_device(L->bias, bias, (size_t)D.E * 4, src_on_device, s) != cudaSuccess))
+    return bail(fail(K3MOE_ERR_CUDA, "router copy failed: %s", cudaGetErrorString(cudaGetLastError())));
+
+  const size_t cn = 3ull * D.f * D.d / 2, cs = 3ull * D.f * D.d / 32;
+  // chunk of experts packed per pass: bounded staging (about 2 GB)
+  int chunk = (int)std::max<size_t>(1, std::min<size_t>(D.E, (size_t)(2ull << 30) / (cn + cs + eb)));
+  uint8_t* stage_nib = nullptr;
+  uint8_t* stage_scl = nullptr;
+  uint8_t* stage_out = nullptr;
+  if (!src_on_device) {
+    if (cudaMalloc(&stage_nib, (size_t)chunk * cn) != cudaSuccess ||
+        cudaMalloc(&stage_scl, (size_t)chunk * cs) != cudaSuccess) {
+      cudaGetLastError();
+      cudaFree(stage_nib);
+      return bail(fail(K3MOE_ERR_OOM, "pack staging allocation failed"));
+    }
+  }
+  bool ok = true;
+  if (!cache) {
+    if (cudaMalloc(&L->packed, (size_t)D.E * eb) != cudaSuccess) {
+      cudaGetLastError();
+      cudaFree(stage_nib);
+      cudaFree(stage_scl);
+      return bail(fail(K3MOE_ERR_OOM, "packed experts: cudaMalloc(%zu) failed", (size_t)D.E * eb));
+    }
+  } else {
+    if (cudaHostAlloc(&L->pool, (size_t)D.E * eb, cudaHostAllocDefault) != cudaSuccess ||
+        cudaHostAlloc((void**)&L->eptr_host, (size_t)D.E * sizeof(void*), cudaHostAllocDefault) != cudaSuccess ||
+        cudaHostAlloc((void**)&L->act_host, (size_t)(D.E + 1) * 4, cudaHostAllocDefault) != cudaSuccess ||
+        cudaMalloc(&stage_out, (size_t)chunk * eb) != cudaSuccess) {
+      cudaGetLastError();
+      cudaFree(stage_nib);
+      cudaFree(stage_scl);
+      cudaFree(stage_out);
+      return bail(fail(K3MOE_ERR_OOM, "pinned expert pool of %zu bytes could not be allocated", (size_t)D.E * eb));
+    }
+    memset((void*)L->eptr_host, 0, (size_t)D.E * sizeof(void*));
+  }
+  for (int e0 = 0; e0 < D.E && ok; e0 += chunk) {
+    const int n = std::min(chunk, D.E - e0);
+    const uint8_t* src_n;
+    const uint8_t* src_s;
+    if (src_on_device) {
+      src_n = (const uint8_t*)canon_nib + (size_t)e0 * cn;
+      src_s = (const uint8_t*)canon_scale + (size_t)e0 * cs;
+    } else {
+      ok = cudaMemcpyAsync(stage_nib, (const uint8_t*)canon_nib + (size_t)e0 * cn, (size_t)n * cn,
+                           cudaMemcpyHostToDevice, s) == cudaSuccess &&
+           cudaMemcpyAsync(stage_scl, (const uint8_t*)canon_scale + (size_t)e0 * cs, (size_t)n * cs,
+                           cudaMemcpyHostToDevice, s) == cudaSuccess;
+      src_n = stage_nib;
+      src_s = stage_scl;
+    }
+    uint8_t* dst = cache ? stage_out : L->packed + (size_t)e0 * eb;
+    ok = ok && launch_pack(src_n, src_s, n, D.d, D.f, dst, L->ws.bad, s) == cudaSuccess;
+    if (ok && cache)
+      ok = cudaMemcpyAsync(L->pool + (size_t)e0 * eb, stage_out, (size_t)n * eb, cudaMemcpyDeviceToHost, s) ==
+           cudaSuccess;
+    if (ok && !src_on_device) ok = cudaStreamSynchronize(s) == cudaSuccess;  // staging reused next chunk
+  }
+  int32_t bad = 0;
+  if (ok) ok = cudaMemcpyAsync(&bad, L->ws.bad, 4, cudaMemcpyDeviceToHost, s) == cudaSuccess;
+  if (ok) ok = cudaStreamSynchronize(s) == cudaSuccess;
+  cudaFree(stage_nib);
+  cudaFree(stage_scl);
+  cudaFree(stage_out);
+  if (!ok) return bail(fail(K3MOE_ERR_CUDA, "packing failed: %s", cudaGetErrorString(cudaGetLastError())));
+  if (bad) return bail(fail(K3MOE_ERR_INVALID_ARG, "a scale byte is 255 (E8M0 NaN)"));
+  if (!cache) {
+    std::vector<const uint8_t*> ptrs(D.E);
+    for (int e = 0; e < D.E; ++e) ptrs[e] = L->packed + (size_t)e * eb;
+    if (cudaMemcpy((void*)L->eptr_dev, ptrs.data(), (size_t)D.E * sizeof(void*), cudaMemcpyHostToDevice) !=
+        cudaSuccess)
+      return bail(fail(K3MOE_ERR_CUDA, "pointer table upload failed"));
+  } else {
+    L->uid = cache->next_uid++;
+    cache->users += 1;
+  }
+  L->last_stream = s;
+  *out = L;
+  return K3MOE_OK;
+}
+
+void k3moe_layer_free(k3moe_layer* L) { free_layer(L); }
+
+int k3moe_router_topk(k3moe_layer* L, const void* x, int T, int32_t* idx, float* w, void* stream) {
+  if (!L || !x || !idx || !w) return fail(K3MOE_ERR_INVALID_ARG, "NULL argument");
+  if (T < 1 || T > L->dims.T_max) return fail(K3MOE_ERR_INVALID_ARG, "T=%d must be in 1..%d", T, L->dims.T_max);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  L->last_stream = s;
+  int rc = run_routing(L, x, T, s);
+  if (rc) return rc;
+  const size_t n = (size_t)T * L->dims.k;
+  CUDA_TRY(cudaMemcpyAsync(idx, L->ws.idx, n * 4, cudaMemcpyDeviceToDevice, s));
+  CUDA_TRY(cudaMemcpyAsync(w, L->ws.w, n * 4, cudaMemcpyDeviceToDevice, s));
+  return K3MOE_OK;
+}
+
+int k3moe_bucket(k3moe_layer* L, const int32_t* idx, int T, int32_t* counts, int32_t* offsets, int32_t* perm,
+                 void* stream) {
+  if (!L || !idx || !counts || !offsets || !perm) return fail(K3MOE_ERR_INVALID_ARG, "NULL argument");
+  if (T < 1 || T > L->dims.T_max) return fail(K3MOE_ERR_INVALID_ARG, "T=%d must be in 1..%d", T, L->dims.T_max);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  L->last_stream = s;
+  const k3moe_dims& D = L->dims;
+  return timed_launch(L, KID_BUCKET, s, [&] {
+    return launch_bucket(idx, T, D.k, D.E, counts, offsets, perm, L->ws.act, L->ws.nact, s);
+  });
+}
+
+int k3moe_layer_forward(k3moe_layer* L, const void* x, int T, float* y, void* stream) {
+  if (!L || !x || !y) return fail(K3MOE_ERR_INVALID_ARG, "NULL argument");
+  if (T < 1 || T > L->dims.T_max) return fail(K3MOE_ERR_INVALID_ARG, "T=%d must be in 1..%d", T, L->dims.T_max);
+  return forward_impl(L, x, T, y, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int k3moe_layer_forward_host(k3moe_layer* L, const void* x_host, int T, float* y_host, void* stream) {
+  if (!L || !x_host || !y_host) return fail(K3MOE_ERR_INVALID_ARG, "NULL argument");
+  if (T < 1 || T > L->dims.T_max) return fail(K3MOE_ERR_INVALID_ARG, "T=%d must be in 1..%d", T, L->dims.T_max);
+  const k3moe_dims& D = L->dims;
+  if (!L->x_stage) {
+    if (cudaMalloc(&L->x_stage, (size_t)D.T_max * D.d * 2) != cudaSuccess ||
+        cudaMalloc(&L->y_stage, (size_t)D.T_max * D.d * 4) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(K3MOE_ERR_OOM, "host-forward staging allocation failed");
+    }
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  CUDA_TRY(cudaMemcpyAsync(L->x_stage, x_host, (size_t)T * D.d * 2, cudaMemcpyHostToDevice, s));
+  int rc = forward_impl(L, L->x_stage, T, L->y_stage, s);
+  if (rc) return rc;
+  CUDA_TRY(cudaMemcpyAsync(y_host, L->y_stage, (size_t)T * D.d * 4, cudaMemcpyDeviceToHost, s));
+  CUDA_TRY(cudaStreamSynchronize(s));
+  return K3MOE_OK;
+}
+
+int k3moe_set_option(k3moe_layer* L, int option, long long value) {
+  if (!L) return fail(K3MOE_ERR_INVALID_ARG, "layer is NULL");
+  switch (option) {
+    case K3MOE_OPT_PATH:
+      if (value != K3MOE_PATH_AUTO && value != K3MOE_PATH_DECODE && value != K3MOE_PATH_GEMM)
+        return fail(K3MOE_ERR_INVALID_ARG, "unknown path %lld", value);
+      L->path = (int)value;
+      return K3MOE_OK;
+    case K3MOE_OPT_GEMM_MIN_T:
+      if (value < 1) return fail(K3MOE_ERR_INVALID_ARG, "GEMM_MIN_T must be >= 1");
+      L->gemm_min_t = value;
+      return K3MOE_OK;
+    default:
+      return fail(K3MOE_ERR_INVALID_ARG, "unknown option %d", option);
+  }
+}
+
+int k3moe_profile(k3moe_layer* L, int enable) {
+  if (!L) return fail(K3MOE_ERR_INVALID_ARG, "layer is NULL");
+  if (L->last_stream) cudaStreamSynchronize(L->last_stream);
+  for (auto& t : L->timed) {
+    L->spare_events.push_back(t.a);
+    L->spare_events.push_back(t.b);
+  }
+  L->timed.clear();
+  for (int i = 0; i < K3MOE_K_COUNT; ++i) {
+    L->prof_ms[i] = 0;
+    L->prof_n[i] = 0;
+  }
+  L->profiling = enable != 0;
+  return K3MOE_OK;
+}
+
+int k3moe_profile_read(k3moe_layer* L, k3moe_kernel_time* out) {
+  if (!L || !out) return fail(K3MOE_ERR_INVALID_ARG, "NULL argument");
+  for (auto& t : L->timed) {
+    float ms = 0.f;
+    CUDA_TRY(cudaEventSynchronize(t.b));
+    CUDA_TRY(cudaEventElapsedTime(&ms, t.a, t.b));
+    L->prof_ms[t.kid] += ms;
+    L->prof_n[t.kid] += 1;
+    L->spare_events.push_back(t.a);
+    L->spare_events.push_back(t.b);
+  }
+  L->timed.clear();
+  for (int i = 0; i < K3MOE_K_COUNT; ++i) {
+    out[i].ms_total = L->prof_ms[i];
+    out[i].launches = L->prof_n[i];
+  }
+  return K3MOE_OK;
+}
+
+int k3moe_read_packed(k3moe_layer* L, int e, void* dst) {
+  if (!L || !dst) return fail(K3MOE_ERR_INVALID_ARG, "NULL argument");
+  if (e < 0 || e >= L->dims.E) return fail(K3MOE_ERR_INVALID_ARG, "expert %d out of range", e);
+  if (L->cache) {
+    memcpy(dst, L->pool + (size_t)e * L->exp_bytes, L->exp_bytes);
+    return K3MOE_OK;
+  }
+  if (L->last_stream) CUDA_TRY(cudaStreamSynchronize(L->last_stream));
+  CUDA_TRY(cudaMemcpy(dst, L->packed + (size_t)e * L->exp_bytes, L->exp_bytes, cudaMemcpyDeviceToHost));
+  return K3MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,111 @@
+// k3moe_internal.cuh -- shared definitions of the CUDA path (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "../../include/k3moe.h"
+
+namespace k3 {
+
+// ----------------------------------------------------------------------------------------
+// Packed MXFP4 layout (the library's own, produced by the pack kernel from the canonical
+// layout; lossless).  A matrix of R rows x K columns (R % 16 == 0, K % 128 == 0) is cut into
+// tiles of 16 rows x 128 columns, stored tile after tile in (row-group, k-tile) order:
+//
+//   tile (rg, kt), 1088 bytes:
+//     [   0,  512)  unit 0: columns 128kt + [0, 64)     16 bytes per lane L = 4g + t (g < 8, t < 4)
+//     [ 512, 1024)  unit 1: columns 128kt + [64, 128)
+//     [1024, 1088)  scales: 8 bytes per g: rows (16rg+g) and (16rg+g+8) x 4 blocks of 32 columns,
+//                   byte 4*h + b = scale of row 16rg + g + 8h, block b
+//   lane L's 16 bytes of unit u: word s (s < 4) holds k16-step s, base column kb = 128kt + 64u + 16s:
+//     byte 0: row g,   columns kb+2t, kb+2t+1        byte 1: row g+8, columns kb+2t, kb+2t+1
+//     byte 2: row g,   columns kb+2t+8, kb+2t+9      byte 3: row g+8, columns kb+2t+8, kb+2t+9
+//     (low nibble = even column), which is exactly the A-operand fragment a0..a7 of
+//     mma.m16n8k16 for that k16 step after an e2m1x2 -> f16x2 conversion of each byte.
+//
+// One expert = [gate/up region][down region]:
+//   gate/up: for rg < f/16, kt < d/128: gate tile (rg, kt) then up tile (rg, kt)
+//   down:    for rg < d/16, kt < f/128: down tile (rg, kt)
+// Total bytes = 3*f*d/2 + 3*f*d/32, the canonical count.
+// ----------------------------------------------------------------------------------------
+constexpr int kTileRows = 16;
+constexpr int kTileCols = 128;
+constexpr int kTileBytes = 1088;
+constexpr int kTileNibBytes = 1024;
+
+__host__ __device__ inline size_t packed_expert_bytes(int d, int f) { return 3ull * (size_t)f * d / 2 + 3ull * (size_t)f * d / 32; }
+__host__ __device__ inline size_t gateup_region_bytes(int d, int f) { return (size_t)(f / 16) * (d / 128) * 2 * kTileBytes; }
+
+// B-operand fragments of the activations (fp16), for one row of K values (x: K = d, h: K = f):
+//   frag[row][blk][t][16 bytes], blk < K/32, t < 4; the 16 bytes hold, for the two k16 steps of
+//   block blk (kb = 32 blk + 16 s, s = 0, 1), the halves (kb+2t, kb+2t+1, kb+2t+8, kb+2t+9):
+//   i.e. registers b0b1, b2b3 of step 0 then of step 1, as mma.m16n8k16 expects for column n.
+// Row stride = K * 2 bytes.
+
+// Workspace of one layer, sized for T_max tokens (P = T_max*k picks).
+struct Workspace {
+  float* logits = nullptr;      // [T_max][E]
+  __half* xfrag = nullptr;      // [T_max][d] fragment order
+  float* xscale = nullptr;      // [T_max] power of two: x = xfrag * xscale
+  int32_t* idx = nullptr;       // [T_max][k]
+  float* w = nullptr;           // [T_max][k]
+  int32_t* counts = nullptr;    // [E]
+  int32_t* offsets = nullptr;   // [E+1]
+  int32_t* perm = nullptr;      // [P]
+  int32_t* act = nullptr;       // [E] active experts in id order
+  int32_t* nact = nullptr;      // [1]
+  __half* hfrag = nullptr;      // [P][f] fragment order
+  float* hscale = nullptr;      // [P][f/32] power of two per (pick, 32-block)
+  float* obuf = nullptr;        // [P][d] w-scaled expert outputs
+  int32_t* arrive = nullptr;    // [T_max][d/64] combine arrival counters (kept at zero)
+  uint32_t* sync = nullptr;     // [8] grid counters (router last-block) + error flags
+  int32_t* bad = nullptr;       // [1] pack-time error flag
+};
+
+enum KernelId {
+  KID_ROUTER = K3MOE_K_ROUTER,
+  KID_TOPK = K3MOE_K_TOPK,
+  KID_BUCKET = K3MOE_K_BUCKET,
+  KID_GATEUP = K3MOE_K_GATEUP,
+  KID_DOWN = K3MOE_K_DOWN,
+  KID_GEMM_GU = K3MOE_K_GEMM_GU,
+  KID_GEMM_DN = K3MOE_K_GEMM_DN,
+  KID_COMBINE = K3MOE_K_COMBINE,
+  KID_GATHER = K3MOE_K_GATHER,
+};
+
+// Kernel launchers (defined in the .cu files).  All return cudaGetLastError().
+struct RouterArgs {
+  const uint16_t* x;      // [T][d] bf16
+  const float* Wr;        // [E][d]
+  const float* bias;      // [E] or nullptr
+  int T, d, E, k;
+  Workspace ws;
+  int fuse_select;        // 1: last block also does top-k + bucketing (small T)
+};
+cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
+cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* idx, float* w,
+                        cudaStream_t s);
+cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* counts, int32_t* offsets,
+                          int32_t* perm, int32_t* act, int32_t* nact, cudaStream_t s);
+
+struct FfnArgs {
+  const uint8_t* const* expert_ptr;  // [E] device pointers to each expert's packed block
+  int d, f, E, k, T;
+  Workspace ws;
+  float* y;                          // [T][d]
+  int max_tasks;                     // grid size bound (active experts are not known on the host)
+};
+cudaError_t launch_gateup(const FfnArgs& a, cudaStream_t s);
+cudaError_t launch_down(const FfnArgs& a, cudaStream_t s);
+
+// canon_nib/canon_scl point at the canonical bytes of the first of n_exp experts; dst at its packed block.
+cudaError_t launch_pack(const uint8_t* canon_nib, const uint8_t* canon_scl, int n_exp, int d, int f, uint8_t* dst,
+                        int32_t* bad, cudaStream_t s);
+
+}  // namespace k3

@@ -1,0 +1,81 @@
+"""The C ABI library loads, exports what include/k3moe.h declares, and refuses bad arguments
+before touching a GPU (these tests need no GPU)."""
+import ctypes
+import re
+
+import pytest
+
+import mxfp4_routed_expert_06_b300 as k3
+
+
+def _declared_functions():
+    src = open(k3.HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(k3moe_\w+)\s*\(", src)))
+
+
+def test_header_and_library_agree():
+    declared = _declared_functions()
+    assert declared == k3.exported_symbols()
+    for name in declared:
+        assert hasattr(k3._lib, name), name
+        assert ctypes.cast(getattr(k3._lib, name), ctypes.c_void_p).value
+
+
+def test_header_constants():
+    assert k3.K3MOE_OK == 0
+    assert k3.K3MOE_ERR_INVALID_ARG == -1 and k3.K3MOE_ERR_BUDGET_TOO_SMALL == -5
+    assert k3.K3MOE_K_COUNT == len(k3.KERNEL_NAMES)
+
+
+@pytest.mark.parametrize("dm,ok", [
+    ((7168, 1536, 896, 16, 1), True),
+    ((256, 128, 8, 2, 4), True),
+    ((7168, 1536, 896, 33, 1), False),   # k > 32
+    ((7168, 1500, 896, 16, 1), False),   # f not a multiple of 128
+    ((100, 128, 8, 2, 4), False),        # d not a multiple of 128
+    ((256, 128, 8, 9, 4), False),        # k > E
+    ((256, 128, 0, 1, 4), False),
+    ((256, 128, 8, 2, 0), False),
+    ((256, 128, 8, 2, 70000), False),
+])
+def test_dims_validation(dm, ok):
+    n = k3.k3moe_packed_expert_bytes(k3.dims(*dm))
+    if ok:
+        d, f = dm[0], dm[1]
+        assert n == 3 * f * d // 2 + 3 * f * d // 32
+    else:
+        assert n == 0
+
+
+def test_k3_packed_size_is_the_pages_count():
+    assert k3.k3moe_packed_expert_bytes(k3.dims(7168, 1536, 896, 16, 1)) == 17_547_264
+
+
+def test_bad_arguments_are_refused_without_device_work():
+    with pytest.raises(k3.K3MoEError) as ei:
+        k3.k3moe_pack_experts(k3.dims(100, 128, 8, 2, 4), 1, 1, 1, 1)
+    assert ei.value.code == k3.K3MOE_ERR_INVALID_ARG and "d=100" in str(ei.value)
+    with pytest.raises(k3.K3MoEError) as ei:
+        k3.k3moe_pack_experts(k3.dims(256, 128, 8, 2, 4), None, 1, 1, 1)
+    assert ei.value.code == k3.K3MOE_ERR_INVALID_ARG
+    with pytest.raises(k3.K3MoEError) as ei:
+        k3.k3moe_pack_experts(k3.dims(256, 128, 8, 2, 4), 1, 1, 2, 1)
+    assert ei.value.code == k3.K3MOE_ERR_INVALID_ARG
+    with pytest.raises(k3.K3MoEError) as ei:
+        k3.k3moe_cache_create(1000, 1024)
+    assert ei.value.code == k3.K3MOE_ERR_INVALID_ARG
+    with pytest.raises(k3.K3MoEError) as ei:
+        k3.k3moe_cache_create(1 << 30, 1000)
+    assert ei.value.code == k3.K3MOE_ERR_INVALID_ARG
+    for fn, args in [(k3.k3moe_layer_forward, (None, 1, 1, 1)), (k3.k3moe_router_topk, (None, 1, 1, 1, 1)),
+                     (k3.k3moe_bucket, (None, 1, 1, 1, 1, 1)), (k3.k3moe_set_option, (None, 1, 0)),
+                     (k3.k3moe_profile, (None, 1))]:
+        with pytest.raises(k3.K3MoEError) as ei:
+            fn(*args)
+        assert ei.value.code == k3.K3MOE_ERR_INVALID_ARG
+
+
+def test_free_null_is_harmless():
+    k3.k3moe_layer_free(None)
+    k3.k3moe_cache_destroy(None)

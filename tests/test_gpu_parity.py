@@ -1,0 +1,295 @@
+"""Parity of the CUDA path (through the C ABI) against the fp64 CPU oracle.
+
+Routing (top-k sets) and bucketing must match exactly; y must be within
+2e-3 * sum|terms| + 1e-5 per element (the bound the layer's accuracy target states).
+Small configurations span several tiles and ragged token counts; the full Kimi K3
+shape (d=7168, f=1536, E=896, k=16) is checked on sampled tokens.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import assert_routing_matches, assert_y_close, gap_filtered_tokens, unpack_tiles
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import mxfp4_routed_expert_06_b300 as k3  # noqa: E402
+
+
+def _dev(a):
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(a).cuda()
+
+
+class Small:
+    """A layer small enough that the oracle runs it whole."""
+
+    def __init__(self, d, f, E, k, T_max, seed=1, bias=None, scale_lo=121, scale_hi=125, nib=None, scl=None):
+        self.d, self.f, self.E, self.k = d, f, E, k
+        self.seed = seed
+        if nib is None:
+            nib, scl = synth.experts(seed, 0, 0, E, d, f, scale_lo, scale_hi)
+        self.nib, self.scl = nib, scl
+        self.Wr = synth.router_weights(seed, 0, E, d)
+        self.bias = bias
+        self.layer = k3.k3moe_pack_experts(k3.dims(d, f, E, k, T_max), nib, scl, 0, self.Wr, bias)
+
+    def tokens(self, T, t0=0):
+        x, _ = gap_filtered_tokens(self.seed, 0, t0, T, self.d, self.Wr, self.bias, self.k)
+        return x
+
+    def forward(self, x):
+        T = x.shape[0]
+        y = torch.empty((T, self.d), dtype=torch.float32, device="cuda")
+        k3.k3moe_layer_forward(self.layer, _dev(x), T, y)
+        torch.cuda.synchronize()
+        return y.cpu().numpy()
+
+    def routing(self, x):
+        T = x.shape[0]
+        idx = torch.empty((T, self.k), dtype=torch.int32, device="cuda")
+        w = torch.empty((T, self.k), dtype=torch.float32, device="cuda")
+        k3.k3moe_router_topk(self.layer, _dev(x), T, idx, w)
+        torch.cuda.synchronize()
+        return idx.cpu().numpy(), w.cpu().numpy()
+
+    def free(self):
+        k3.k3moe_layer_free(self.layer)
+
+
+def _check_layer(L: Small, x, what):
+    ref = oracle.layer(x, L.Wr, L.bias, L.k, L.f, L.nib, L.scl)
+    idx, w = L.routing(x)
+    assert_routing_matches(idx, w, ref["idx"], ref["w"], ref["keys"])
+    y = L.forward(x)
+    return assert_y_close(y, ref["y"], ref["sumabs"], what)
+
+
+def test_device_generator_matches_host():
+    for d, f, e0, e1 in [(256, 128, 0, 3), (7168, 1536, 895, 896)]:
+        nb, sb = synth.expert_bytes(d, f)
+        n = e1 - e0
+        dn = torch.empty(n * nb, dtype=torch.uint8, device="cuda")
+        ds = torch.empty(n * sb, dtype=torch.uint8, device="cuda")
+        synth.experts_to_device(7, 2, e0, e1, d, f, dn.data_ptr(), ds.data_ptr())
+        torch.cuda.synchronize()
+        hn, hs = synth.experts(7, 2, e0, e1, d, f)
+        assert np.array_equal(dn.cpu().numpy(), hn.reshape(-1))
+        assert np.array_equal(ds.cpu().numpy(), hs.reshape(-1))
+
+
+def test_pack_layout_round_trip():
+    L = Small(256, 128, 8, 2, 4)
+    nb = k3.k3moe_packed_expert_bytes(k3.dims(256, 128, 8, 2, 4))
+    for e in range(8):
+        buf = np.empty(nb, np.uint8)
+        k3.k3moe_read_packed(L.layer, e, buf)
+        n, s = unpack_tiles(buf, 256, 128)
+        assert np.array_equal(n, L.nib[e]) and np.array_equal(s, L.scl[e])
+    L.free()
+
+
+def test_tiny_config_c1():
+    # d=256, f=128, E=8, k=2, T=4, no bias: the smallest configuration, run whole.
+    L = Small(256, 128, 8, 2, 4)
+    x = L.tokens(4)
+    ref = oracle.layer(x, L.Wr, None, 2, 128, L.nib, L.scl)
+    idx, w = L.routing(x)
+    assert_routing_matches(idx, w, ref["idx"], ref["w"], ref["keys"])
+    # bucketing entry point on the same picks
+    counts = torch.empty(8, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(9, dtype=torch.int32, device="cuda")
+    perm = torch.empty(8, dtype=torch.int32, device="cuda")
+    k3.k3moe_bucket(L.layer, _dev(idx), 4, counts, offsets, perm)
+    torch.cuda.synchronize()
+    c_o, o_o, p_o = oracle.bucket(idx, 8)
+    assert counts.cpu().numpy().tolist() == c_o.tolist()
+    assert offsets.cpu().numpy().tolist() == o_o.tolist()
+    assert perm.cpu().numpy().tolist() == p_o.tolist()
+    y = L.forward(x)
+    assert_y_close(y, ref["y"], ref["sumabs"], "C1")
+    L.free()
+
+
+@pytest.mark.parametrize("d,f,E,k,T", [
+    (512, 256, 16, 4, 1),
+    (512, 256, 16, 4, 3),
+    (384, 384, 32, 8, 17),
+    (1024, 512, 64, 6, 64),
+    (384, 128, 12, 3, 129),
+    (512, 256, 40, 9, 120),   # 1080 picks: separate top-k and bucketing kernels
+])
+def test_small_configs(d, f, E, k, T):
+    L = Small(d, f, E, k, T, seed=d + f + E + k + T)
+    _check_layer(L, L.tokens(T), f"d{d} f{f} E{E} k{k} T{T}")
+    L.free()
+
+
+def test_bias_steers_selection_hot_expert():
+    # a +10 bias on expert 3 with k=1: every token picks expert 3 (40 tokens > 8 per pass),
+    # and its combine weight is 1 (sigmoid of the unbiased logit, renormalised).
+    d, f, E = 256, 128, 8
+    bias = np.zeros(E, np.float32)
+    bias[3] = 10.0
+    L = Small(d, f, E, 1, 40, seed=5, bias=bias)
+    x = L.tokens(40)
+    idx, w = L.routing(x)
+    assert np.all(idx == 3) and np.all(w == 1.0)
+    _check_layer(L, x, "hot expert")
+    L.free()
+
+
+def test_hot_subset_bias_k3():
+    d, f, E, k = 512, 256, 24, 4
+    bias = synth.hot_bias(9, 0, E, 6, 2.0)
+    L = Small(d, f, E, k, 33, seed=9, bias=bias)
+    x = L.tokens(33)
+    idx, _ = L.routing(x)
+    assert set(np.unique(idx)) <= set(np.nonzero(bias)[0].tolist())
+    _check_layer(L, x, "hot subset")
+    L.free()
+
+
+def test_zero_nibbles_give_zero_output():
+    d, f, E, k = 256, 128, 8, 2
+    nb, sb = synth.expert_bytes(d, f)
+    nib = np.zeros((E, nb), np.uint8)
+    nib[:, : nb // 3] = 0x88  # gate all -0
+    scl = np.full((E, sb), 123, np.uint8)
+    L = Small(d, f, E, k, 5, nib=nib, scl=scl)
+    y = L.forward(L.tokens(5))
+    assert np.all(y == 0)
+    L.free()
+
+
+@pytest.mark.parametrize("lo,hi", [(121, 121), (125, 125), (110, 135)])
+def test_scale_extremes(lo, hi):
+    L = Small(256, 256, 8, 2, 6, seed=lo * hi, scale_lo=lo, scale_hi=hi)
+    _check_layer(L, L.tokens(6), f"scales {lo}..{hi}")
+    L.free()
+
+
+def test_nan_scale_refused():
+    d, f, E = 256, 128, 4
+    nib, scl = synth.experts(1, 0, 0, E, d, f)
+    scl[2, 17] = 255
+    Wr = synth.router_weights(1, 0, E, d)
+    with pytest.raises(k3.K3MoEError) as ei:
+        k3.k3moe_pack_experts(k3.dims(d, f, E, 2, 4), nib, scl, 0, Wr)
+    assert ei.value.code == k3.K3MOE_ERR_INVALID_ARG
+
+
+def test_bucket_entry_point_large():
+    E, k, T = 64, 8, 300
+    L = Small(256, 128, E, k, T)
+    rng = np.random.default_rng(3)
+    idx = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    perm = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    k3.k3moe_bucket(L.layer, _dev(idx), T, counts, offsets, perm)
+    torch.cuda.synchronize()
+    c_o, o_o, p_o = oracle.bucket(idx, E)
+    assert np.array_equal(counts.cpu().numpy(), c_o)
+    assert np.array_equal(offsets.cpu().numpy(), o_o)
+    assert np.array_equal(perm.cpu().numpy(), p_o)
+    L.free()
+
+
+def test_deterministic_and_host_entry_point():
+    L = Small(512, 256, 16, 4, 9)
+    x = L.tokens(9)
+    y1 = L.forward(x)
+    y2 = L.forward(x)
+    assert np.array_equal(y1, y2)
+    yh = np.empty((9, 512), np.float32)
+    k3.k3moe_layer_forward_host(L.layer, np.ascontiguousarray(x), 9, yh)
+    assert np.array_equal(yh, y1)
+    L.free()
+
+
+# ------------------------------------------------------------------ Kimi K3 shape ---
+
+K3D, K3F, K3E, K3K = 7168, 1536, 896, 16
+SEED = 2026
+
+
+@pytest.fixture(scope="module")
+def k3_layer():
+    """One full K3-shaped layer: 896 experts generated on the device, packed, 15.7 GB resident."""
+    nb, sb = synth.expert_bytes(K3D, K3F)
+    dn = torch.empty(K3E * nb, dtype=torch.uint8, device="cuda")
+    ds = torch.empty(K3E * sb, dtype=torch.uint8, device="cuda")
+    synth.experts_to_device(SEED, 0, 0, K3E, K3D, K3F, dn.data_ptr(), ds.data_ptr())
+    Wr = synth.router_weights(SEED, 0, K3E, K3D)
+    layer = k3.k3moe_pack_experts(k3.dims(K3D, K3F, K3E, K3K, 64), dn, ds, 1, _dev(Wr), None)
+    del dn, ds
+    torch.cuda.empty_cache()
+    yield layer, Wr
+    k3.k3moe_layer_free(layer)
+
+
+def _k3_oracle_y(x, idx, w):
+    """Oracle y for K3-shaped tokens; the experts are regenerated on the host one by one."""
+    cache = {}
+    nibs, scls = [], []
+    for e in idx.reshape(-1).tolist():
+        if e not in cache:
+            n, s = synth.experts(SEED, 0, e, e + 1, K3D, K3F)
+            cache[e] = (n[0], s[0])
+        nibs.append(cache[e][0])
+        scls.append(cache[e][1])
+    return oracle.moe(x, w, nibs, scls, K3F)
+
+
+def _run(layer, x):
+    T = x.shape[0]
+    y = torch.empty((T, K3D), dtype=torch.float32, device="cuda")
+    idx = torch.empty((T, K3K), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, K3K), dtype=torch.float32, device="cuda")
+    k3.k3moe_router_topk(layer, _dev(x), T, idx, w)
+    k3.k3moe_layer_forward(layer, _dev(x), T, y)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), w.cpu().numpy(), y.cpu().numpy()
+
+
+def test_k3_single_token_decode(k3_layer):
+    # the single-token decode workload: T = 1 calls, as the benchmark times them
+    layer, Wr = k3_layer
+    x, _ = gap_filtered_tokens(SEED, 0, 0, 3, K3D, Wr, None, K3K)
+    for t in range(3):
+        xt = x[t:t + 1]
+        idx, w, y = _run(layer, xt)
+        i_o, w_o, _, keys = oracle.router(xt, Wr, None, K3K)
+        assert_routing_matches(idx, w, i_o, w_o, keys)
+        y_o, sa = _k3_oracle_y(xt, i_o, w_o)
+        assert_y_close(y, y_o, sa, f"K3 T=1 token {t}")
+
+
+def test_k3_batched_decode_t64(k3_layer):
+    layer, Wr = k3_layer
+    T = 64
+    x, _ = gap_filtered_tokens(SEED, 0, 1000, T, K3D, Wr, None, K3K)
+    idx, w, y = _run(layer, x)
+    i_o, w_o, _, keys = oracle.router(x, Wr, None, K3K)
+    assert_routing_matches(idx, w, i_o, w_o, keys)
+    # bucketing of all 1024 picks, exact
+    counts = torch.empty(K3E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(K3E + 1, dtype=torch.int32, device="cuda")
+    perm = torch.empty(T * K3K, dtype=torch.int32, device="cuda")
+    k3.k3moe_bucket(layer, _dev(idx), T, counts, offsets, perm)
+    torch.cuda.synchronize()
+    c_o, o_o, p_o = oracle.bucket(idx, K3E)
+    assert np.array_equal(counts.cpu().numpy(), c_o) and np.array_equal(perm.cpu().numpy(), p_o)
+    assert np.array_equal(offsets.cpu().numpy(), o_o)
+    # y on sampled tokens: first, last and one in between
+    for t in (0, 37, T - 1):
+        y_o, sa = _k3_oracle_y(x[t:t + 1], i_o[t:t + 1], w_o[t:t + 1])
+        assert_y_close(y[t:t + 1], y_o, sa, f"K3 T=64 token {t}")
+    # whole-batch invariant at any size: bitwise repeatable
+    _, _, y2 = _run(layer, x)
+    assert np.array_equal(y, y2)
