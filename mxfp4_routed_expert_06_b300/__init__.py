@@ -9,7 +9,7 @@ else the legacy default stream).
 
 No computation happens in Python: every step of the layer runs in the library's CUDA
 kernels.  The package refuses to import when ``libk3moe.so`` has not been built
-(``python -m mxfp4_routed_expert_06_b300.build``); there is no fallback.
+(``python mxfp4_routed_expert_06_b300/build.py``); there is no fallback.
 """
 from __future__ import annotations
 
@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(_HERE, "libk3moe.so")
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "k3moe.h")
 
 if not os.path.exists(LIB_PATH):
-    raise ImportError(f"{LIB_PATH} is missing: build it with `python -m mxfp4_routed_expert_06_b300.build`")
+    raise ImportError(f"{LIB_PATH} is missing: build it with `python mxfp4_routed_expert_06_b300/build.py`")
 
 _lib = ctypes.CDLL(LIB_PATH)
 

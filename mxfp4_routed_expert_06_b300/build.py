@@ -1,6 +1,7 @@
 """Build libk3moe.so (the CUDA path and its C ABI) in-tree for sm_103a.
 
-Usage: ``python -m mxfp4_routed_expert_06_b300.build [--force]``.  nvcc cross-compiles
+Usage: ``python mxfp4_routed_expert_06_b300/build.py [--force]`` (run it by path: importing
+the package itself needs the built library).  nvcc cross-compiles
 without a GPU, so this also runs on a CPU-only machine.
 """
 from __future__ import annotations
