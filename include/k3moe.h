@@ -111,6 +111,28 @@ int k3moe_pack_experts(const k3moe_dims* dims, const void* canon_nib, const void
  * Errors: INVALID_ARG, CUDA. */
 int k3moe_router_topk(k3moe_layer* layer, const void* x_bf16, int T, int32_t* idx, float* w, void* stream);
 
+/* Router + top-k without any device allocation, and without a layer object.  The pages
+ * have no counterpart: this entry point exists for callers that cannot call cudaMalloc --
+ * code running inside a host framework whose memory pool already owns the device memory
+ * (another allocation may fail or bypass the framework's accounting), or loops where an
+ * allocation's implicit device synchronisation is not acceptable.  It computes exactly what
+ * k3moe_router_topk computes (same kernels' arithmetic, bitwise the same idx and w), from
+ * caller buffers:
+ *   x     device, [T][d] bf16 (8-byte aligned);  W_r device, [E][d] float32 (16-byte aligned)
+ *   bias  device, [E] float32, or NULL;  idx device, [T][k] int32;  w device, [T][k] float32
+ *   d multiple of 4; 1 <= E <= 4096; 1 <= k <= min(E, 32); T*E <= 65536 (larger requests are
+ *   refused with K3MOE_ERR_INVALID_ARG).
+ * Its scratch (the T*E router logits and a block-election ticket) is one fixed 256 KiB + 256 B
+ * array in the library's device memory, held by every GPU that loads the library until the
+ * process exits.  The first call on a device does a one-time set-up with that device current
+ * (it looks up the array's device address); make that first call before any stream capture.
+ * Every call on a device shares the array, which keeps the previous call's contents; the
+ * ticket is cleared on `stream` before each launch.  Calls that overlap on the GPU (on two
+ * streams at once) race on the array and give undefined results.
+ * Errors: INVALID_ARG, CUDA. */
+int k3moe_router_topk_noalloc(const void* x_bf16, const float* W_r, const float* bias, int T, int d, int E, int k,
+                              int32_t* idx, float* w, void* stream);
+
 /* Token-to-expert bucketing of T*k picks (pick p = t*k + slot):
  *   counts[e]  number of picks routed to expert e                      [E] int32
  *   offsets    exclusive prefix sum of counts in expert-id order       [E+1] int32

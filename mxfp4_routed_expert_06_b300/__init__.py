@@ -73,6 +73,7 @@ _SIGS = {
     "k3moe_cache_reset_stats": ([_vp], _i),
     "k3moe_cache_destroy": ([_vp], None),
     "k3moe_last_error": ([], ctypes.c_char_p),
+    "k3moe_router_topk_noalloc": ([_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp], _i),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -181,6 +182,11 @@ def k3moe_read_packed(layer, e: int, dst) -> None:
 
 def k3moe_layer_free(layer) -> None:
     _lib.k3moe_layer_free(_handle(layer))
+
+
+def k3moe_router_topk_noalloc(x, W_r, bias, T: int, d: int, E: int, k: int, idx, w, stream=None) -> None:
+    _check(_lib.k3moe_router_topk_noalloc(_ptr(x), _ptr(W_r), _ptr(bias), T, d, E, k, _ptr(idx), _ptr(w),
+                                          _stream(stream)))
 
 
 def k3moe_cache_create(budget_bytes: int, slot_bytes: int):

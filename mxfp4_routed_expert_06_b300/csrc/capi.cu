@@ -59,6 +59,8 @@ struct TimedLaunch {
 
 }  // namespace
 
+void k3::set_last_error(const char* msg) { g_err = msg; }
+
 struct k3moe_cache {
   size_t slot_bytes = 0;
   int n_slots = 0;

@@ -108,4 +108,7 @@ cudaError_t launch_down(const FfnArgs& a, cudaStream_t s);
 cudaError_t launch_pack(const uint8_t* canon_nib, const uint8_t* canon_scl, int n_exp, int d, int f, uint8_t* dst,
                         int32_t* bad, cudaStream_t s);
 
+// Sets the message k3moe_last_error() returns on this thread.
+void set_last_error(const char* msg);
+
 }  // namespace k3
