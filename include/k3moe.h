@@ -163,9 +163,21 @@ int k3moe_layer_forward(k3moe_layer* layer, const void* x_bf16, int T, float* y,
  * memory gives the fastest copies; pageable memory also works.  Errors as layer_forward. */
 int k3moe_layer_forward_host(k3moe_layer* layer, const void* x_bf16_host, int T, float* y_host, void* stream);
 
+/* Synchronise the layer's last stream and report device-side failures: every wait inside
+ * the kernels is bounded (K3MOE_OPT_DEVICE_WAIT_NS, default 2 s); a wait that gives up sets a
+ * device flag and its kernel returns early.  This call returns K3MOE_ERR_TIMEOUT (and clears the
+ * flag) if that happened since the previous check; the outputs of those calls are invalid.
+ * k3moe_layer_forward_host does the same check itself. */
+int k3moe_sync(k3moe_layer* layer);
+
 /* Options. */
 #define K3MOE_OPT_PATH 1        /* value: K3MOE_PATH_AUTO (default), _DECODE, _GEMM */
 #define K3MOE_OPT_GEMM_MIN_T 2  /* value: smallest T the AUTO path sends to the grouped GEMM */
+#define K3MOE_OPT_DEVICE_WAIT_NS 3  /* value: bound in ns on every device-side wait (1e6..6e10) */
+#define K3MOE_OPT_TEST_STALL 4  /* value 1: the next forward's FFN kernels wait on a barrier that
+                                   nothing completes until the bound expires (failure-path test) */
+#define K3MOE_OPT_RING_DEPTH 5  /* value 0 (default): automatic; 1..6: stages each streaming warp
+                                   keeps in flight (a tuning and test knob; results do not change) */
 #define K3MOE_PATH_AUTO 0
 #define K3MOE_PATH_DECODE 1
 #define K3MOE_PATH_GEMM 2
@@ -197,6 +209,12 @@ int k3moe_profile_read(k3moe_layer* layer, k3moe_kernel_time* out);
 /* Copy expert e's packed bytes (k3moe_packed_expert_bytes) to host memory `dst`;
  * synchronous.  For layout checks. */
 int k3moe_read_packed(k3moe_layer* layer, int e, void* dst);
+
+/* Diagnostics: device address and size of an internal buffer of the last call (read only;
+ * valid until the layer's next call or free).  which: 0 = SwiGLU output h, fp32 [T_max*k][f];
+ * 1 = per-pick expert outputs times the combine weight, fp32 [T_max*k][d]; 2 = the routed
+ * expert ids, int32 [T_max][k]. */
+int k3moe_debug_buffer(k3moe_layer* layer, int which, void** dev_ptr, size_t* bytes);
 
 void k3moe_layer_free(k3moe_layer* layer);
 

@@ -64,9 +64,11 @@ _SIGS = {
     "k3moe_layer_forward": ([_vp, _vp, _i, _vp, _vp], _i),
     "k3moe_layer_forward_host": ([_vp, _vp, _i, _vp, _vp], _i),
     "k3moe_set_option": ([_vp, _i, ctypes.c_longlong], _i),
+    "k3moe_sync": ([_vp], _i),
     "k3moe_profile": ([_vp, _i], _i),
     "k3moe_profile_read": ([_vp, ctypes.POINTER(k3moe_kernel_time)], _i),
     "k3moe_read_packed": ([_vp, _i, _vp], _i),
+    "k3moe_debug_buffer": ([_vp, _i, ctypes.POINTER(_vp), ctypes.POINTER(_sz)], _i),
     "k3moe_layer_free": ([_vp], None),
     "k3moe_cache_create": ([_sz, _sz, ctypes.POINTER(_vp)], _i),
     "k3moe_cache_stats": ([_vp, ctypes.POINTER(k3moe_cache_stats_t)], _i),
@@ -162,6 +164,10 @@ def k3moe_layer_forward_host(layer, x_host, T: int, y_host, stream=None) -> None
     _check(_lib.k3moe_layer_forward_host(_handle(layer), _ptr(x_host), T, _ptr(y_host), _stream(stream)))
 
 
+def k3moe_sync(layer) -> None:
+    _check(_lib.k3moe_sync(_handle(layer)))
+
+
 def k3moe_set_option(layer, option: int, value: int) -> None:
     _check(_lib.k3moe_set_option(_handle(layer), option, value))
 
@@ -178,6 +184,12 @@ def k3moe_profile_read(layer) -> dict:
 
 def k3moe_read_packed(layer, e: int, dst) -> None:
     _check(_lib.k3moe_read_packed(_handle(layer), e, _ptr(dst)))
+
+
+def k3moe_debug_buffer(layer, which: int) -> tuple[int, int]:
+    ptr, n = ctypes.c_void_p(), ctypes.c_size_t()
+    _check(_lib.k3moe_debug_buffer(_handle(layer), which, ctypes.byref(ptr), ctypes.byref(n)))
+    return ptr.value, n.value
 
 
 def k3moe_layer_free(layer) -> None:

@@ -32,15 +32,18 @@ def stale() -> bool:
     return any(os.path.getmtime(p) > t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and not stale():
+def build(force: bool = False, verbose: bool = False, checks: bool = False) -> str:
+    """checks=True builds the self-checking variant (K3MOE_DEVICE_CHECKS): device-side copy
+    addresses are checked and a failure is recorded and skipped instead of faulting."""
+    if not force and not checks and not stale():
         return LIB
     objdir = os.path.join(HERE, "_build")
     os.makedirs(objdir, exist_ok=True)
     objs = []
     for src in SOURCES:
         obj = os.path.join(objdir, src.replace(".cu", ".o"))
-        cmd = ["nvcc", *NVCC_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = ["nvcc", *NVCC_FLAGS, *(["-DK3MOE_DEVICE_CHECKS"] if checks else []), "-c", os.path.join(CSRC, src),
+               "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         subprocess.check_call(cmd)
@@ -53,5 +56,6 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose="-v" in sys.argv)
+    build(force="--force" in sys.argv or "--checks" in sys.argv, verbose="-v" in sys.argv,
+          checks="--checks" in sys.argv)
     print(LIB)

@@ -102,6 +102,10 @@ struct k3moe_layer {
   cudaEvent_t copies_done = nullptr;
   uint16_t* x_stage = nullptr;  // forward_host staging
   float* y_stage = nullptr;
+  int num_sms = 148;
+  unsigned long long wait_ns = 2000000000ull;  // bound on device-side waits
+  int test_stall = 0;                           // next forward stalls its FFN consumers (timeout test)
+  int ring_depth = 0;                           // 0: automatic
 };
 
 namespace {
@@ -147,9 +151,10 @@ int alloc_workspace(k3moe_layer* L) {
       {(void**)&w.logits, T * D.E * 4},  {(void**)&w.xfrag, T * D.d * 2},       {(void**)&w.xscale, T * 4},
       {(void**)&w.idx, P * 4},           {(void**)&w.w, P * 4},                 {(void**)&w.counts, (size_t)D.E * 4},
       {(void**)&w.offsets, (size_t)(D.E + 1) * 4}, {(void**)&w.perm, P * 4},    {(void**)&w.act, (size_t)D.E * 4},
-      {(void**)&w.nact, 4},              {(void**)&w.hfrag, P * D.f * 2},       {(void**)&w.hscale, P * (D.f / 32) * 4},
-      {(void**)&w.obuf, P * D.d * 4},    {(void**)&w.arrive, T * (D.d / 64) * 4}, {(void**)&w.sync, 64},
-      {(void**)&w.bad, 4},
+      {(void**)&w.nact, 4},              {(void**)&w.units, (P / kUnitTokens + D.E + 1) * sizeof(UnitDesc)},
+      {(void**)&w.nunits, 4},            {(void**)&w.hbuf, P * D.f * 4},        {(void**)&w.pair, P * (D.f / 32) * 4},
+      {(void**)&w.hfrag, P * D.f * 2},   {(void**)&w.hscale, P * (D.f / 32) * 4},
+      {(void**)&w.obuf, P * D.d * 4},    {(void**)&w.sync, 64},                 {(void**)&w.bad, 4},
   };
   size_t total = 0;
   for (auto& it : items) total += align256(it.bytes);
@@ -199,6 +204,16 @@ void free_layer(k3moe_layer* L) {
   delete L;
 }
 
+// After a kernel gave up part-way, clear the error flags and the per-call counters that a
+// completed call leaves at zero.
+cudaError_t reset_after_timeout(k3moe_layer* L) {
+  const k3moe_dims& D = L->dims;
+  cudaError_t e = cudaMemset(L->ws.sync, 0, 64);
+  if (e == cudaSuccess) e = cudaMemset(L->ws.pair, 0, (size_t)D.T_max * D.k * (D.f / 32) * 4);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  return e;
+}
+
 bool use_gemm(const k3moe_layer* L, int T) {
   if (L->path == K3MOE_PATH_GEMM) return true;
   if (L->path == K3MOE_PATH_DECODE) return false;
@@ -218,7 +233,7 @@ int run_routing(k3moe_layer* L, const void* x, int T, cudaStream_t s) {
     if (rc) return rc;
     rc = timed_launch(L, KID_BUCKET, s, [&] {
       return launch_bucket(L->ws.idx, T, D.k, D.E, L->ws.counts, L->ws.offsets, L->ws.perm, L->ws.act, L->ws.nact,
-                           s);
+                           L->ws.units, L->ws.nunits, L->ws.w, L->ws.xscale, s);
     });
     if (rc) return rc;
   }
@@ -299,10 +314,13 @@ int forward_impl(k3moe_layer* L, const void* x, int T, float* y, cudaStream_t s)
     rc = make_resident(L, s);
     if (rc) return rc;
   }
-  FfnArgs fa{L->eptr_dev, D.d, D.f, D.E, D.k, T, L->ws, y, std::min(D.E, T * D.k)};
+  FfnArgs fa{L->eptr_dev, D.d, D.f, D.E, D.k, T, L->ws, y, L->num_sms, L->wait_ns, L->test_stall, L->ring_depth};
+  L->test_stall = 0;
   rc = timed_launch(L, KID_GATEUP, s, [&] { return launch_gateup(fa, s); });
   if (rc) return rc;
-  return timed_launch(L, KID_DOWN, s, [&] { return launch_down(fa, s); });
+  rc = timed_launch(L, KID_DOWN, s, [&] { return launch_down(fa, s); });
+  if (rc) return rc;
+  return timed_launch(L, KID_COMBINE, s, [&] { return launch_combine(fa, s); });
 }
 
 }  // namespace
@@ -403,6 +421,13 @@ int k3moe_pack_experts(const k3moe_dims* dims, const void* canon_nib, const void
   L->dims = D;
   L->exp_bytes = eb;
   L->cache = cache;
+  {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+        n > 0)
+      L->num_sms = n;
+    cudaGetLastError();
+  }
   auto bail = [&](int code) {
     free_layer(L);
     return code;
@@ -523,7 +548,8 @@ int k3moe_bucket(k3moe_layer* L, const int32_t* idx, int T, int32_t* counts, int
   L->last_stream = s;
   const k3moe_dims& D = L->dims;
   return timed_launch(L, KID_BUCKET, s, [&] {
-    return launch_bucket(idx, T, D.k, D.E, counts, offsets, perm, L->ws.act, L->ws.nact, s);
+    return launch_bucket(idx, T, D.k, D.E, counts, offsets, perm, L->ws.act, L->ws.nact, L->ws.units, L->ws.nunits,
+                         L->ws.w, L->ws.xscale, s);
   });
 }
 
@@ -550,12 +576,45 @@ int k3moe_layer_forward_host(k3moe_layer* L, const void* x_host, int T, float* y
   if (rc) return rc;
   CUDA_TRY(cudaMemcpyAsync(y_host, L->y_stage, (size_t)T * D.d * 4, cudaMemcpyDeviceToHost, s));
   CUDA_TRY(cudaStreamSynchronize(s));
+  uint32_t flags = 0;
+  CUDA_TRY(cudaMemcpy(&flags, L->ws.sync + 1, 4, cudaMemcpyDeviceToHost));
+  if (flags) {
+    CUDA_TRY(reset_after_timeout(L));
+    return fail(K3MOE_ERR_TIMEOUT, "a device-side wait gave up (flags 0x%x)", flags);
+  }
+  return K3MOE_OK;
+}
+
+int k3moe_sync(k3moe_layer* L) {
+  if (!L) return fail(K3MOE_ERR_INVALID_ARG, "layer is NULL");
+  if (L->last_stream) CUDA_TRY(cudaStreamSynchronize(L->last_stream));
+  CUDA_TRY(cudaDeviceSynchronize());
+  uint32_t flags = 0;
+  CUDA_TRY(cudaMemcpy(&flags, L->ws.sync + 1, 4, cudaMemcpyDeviceToHost));
+  if (flags) {
+    CUDA_TRY(reset_after_timeout(L));
+    return fail(K3MOE_ERR_TIMEOUT, "a device-side wait gave up (flags 0x%x); the results of the calls since the "
+                "last k3moe_sync are invalid", flags);
+  }
   return K3MOE_OK;
 }
 
 int k3moe_set_option(k3moe_layer* L, int option, long long value) {
   if (!L) return fail(K3MOE_ERR_INVALID_ARG, "layer is NULL");
   switch (option) {
+    case K3MOE_OPT_DEVICE_WAIT_NS:
+      if (value < 1000000 || value > 60000000000LL)
+        return fail(K3MOE_ERR_INVALID_ARG, "DEVICE_WAIT_NS must be in 1e6..6e10");
+      L->wait_ns = (unsigned long long)value;
+      return K3MOE_OK;
+    case K3MOE_OPT_RING_DEPTH:
+      if (value < 0 || value > 6) return fail(K3MOE_ERR_INVALID_ARG, "RING_DEPTH must be in 0..6");
+      L->ring_depth = (int)value;
+      return K3MOE_OK;
+    case K3MOE_OPT_TEST_STALL:
+      if (value != 0 && value != 1) return fail(K3MOE_ERR_INVALID_ARG, "TEST_STALL must be 0 or 1");
+      L->test_stall = (int)value;
+      return K3MOE_OK;
     case K3MOE_OPT_PATH:
       if (value != K3MOE_PATH_AUTO && value != K3MOE_PATH_DECODE && value != K3MOE_PATH_GEMM)
         return fail(K3MOE_ERR_INVALID_ARG, "unknown path %lld", value);
@@ -603,6 +662,18 @@ int k3moe_profile_read(k3moe_layer* L, k3moe_kernel_time* out) {
     out[i].launches = L->prof_n[i];
   }
   return K3MOE_OK;
+}
+
+int k3moe_debug_buffer(k3moe_layer* L, int which, void** dev_ptr, size_t* bytes) {
+  if (!L || !dev_ptr || !bytes) return fail(K3MOE_ERR_INVALID_ARG, "NULL argument");
+  const k3moe_dims& D = L->dims;
+  const size_t P = (size_t)D.T_max * D.k;
+  switch (which) {
+    case 0: *dev_ptr = L->ws.hbuf; *bytes = P * D.f * 4; return K3MOE_OK;
+    case 1: *dev_ptr = L->ws.obuf; *bytes = P * D.d * 4; return K3MOE_OK;
+    case 2: *dev_ptr = L->ws.idx; *bytes = P * 4; return K3MOE_OK;
+    default: return fail(K3MOE_ERR_INVALID_ARG, "unknown buffer %d", which);
+  }
 }
 
 int k3moe_read_packed(k3moe_layer* L, int e, void* dst) {

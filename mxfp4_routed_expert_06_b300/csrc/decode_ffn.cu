@@ -2,25 +2,98 @@
 //
 // "kimi-k3-in-c deep dive", "four reductions", reduction 1: the experts stay MXFP4 and are
 // multiplied on the nibbles, never expanded to a dense copy (value = E2M1[nibble] *
-// 2^(scale-127), 32 values per scale).  On the GPU each expert's bytes are streamed from HBM
-// exactly once per call, each lane's 16-byte chunk is turned into four f16x2 A fragments per
-// word with the hardware e2m1x2 -> f16x2 conversion, and mma.m16n8k16 multiplies them with
-// up to 8 routed tokens at a time (tokens are the n = 8 columns).  The E8M0 scale of a
-// 32-column block is applied once per block: the block's two k16 steps accumulate into a
-// zeroed fp32 fragment that is then added, times the scale, to the running fp32 sum.  Every
-// product is exact (fp16 x fp16 into fp32) and all sums are fp32.
+// 2^(scale-127), 32 values per scale).  Here every routed expert's bytes stream from HBM once
+// per call into shared memory (per-warp cp.async rings, L2 evict-first), and consumer warps
+// turn each byte into an f16x2 tensor-core
+// fragment with the hardware e2m1x2 -> f16x2 conversion and multiply with mma.m16n8k16,
+// the routed tokens of one work unit (<= 8) being the n = 8 columns.  The E8M0 scale of each
+// 32-column block is applied once per block in fp32: the block's two k16 steps accumulate
+// into a zeroed fp32 fragment that is added, times the scale, to the running sum.  fp16 x
+// fp16 products are exact and every sum is fp32.
 //
-//   gateup_kernel: CTA = (routed expert, 32 rows of f); 8 warps split d; the partial sums
-//                  are added in warp order, then h = silu(g) * u (SwiGLU) is stored as fp16
-//                  B fragments with one power-of-two scale per (pick, 32 rows).
-//   down_kernel:   CTA = (routed expert, 64 rows of d); 4 row groups x 2 halves of f; the
-//                  outputs times the combine weight go to obuf[pick]; the last of a token's
-//                  k picks to finish a 64-row chunk sums the k slots in slot order into y
-//                  (fixed reduction order, independent of which CTA finishes last).
+// Both FFN kernels are persistent (one CTA per SM); a CTA walks tasks
+// i = blockIdx.x + j*gridDim.x.  Each consumer warp streams its own stages from HBM with
+// cp.async (16 bytes per lane, L2 evict-first) several stages ahead into a private shared-memory
+// ring; on this GPU that keeps ~7 TB/s in flight, where a single-thread bulk-copy producer is
+// limited by a per-copy cost.
+//   gateup_kernel  task = (unit, 16 rows of f); stage = one 128-column k-tile of the gate and
+//                  up tiles (2176 B) + the unit's x fragments for it; consumer warp w takes
+//                  k-tiles kt % 8 == w; one of 4 epilogue warps adds the 8 partial sums in
+//                  warp order, applies SwiGLU h = silu(g) * u, and the second of the two 16-row
+//                  halves of a 32-row block to finish converts that block of h to fp16
+//                  fragments with one power-of-two scale per (pick, 32 rows).
+//   down_kernel    task = (unit, 16 rows of d) over the whole f range, streamed in chunks of
+//                  k-tiles; consumer warp = task % 8; writes w * o to obuf[pick].
+//   combine_kernel y[t] = sum over the k slots, in slot order, of obuf[t*k + slot].
+// Every device-side wait is bounded (globaltimer); on expiry the kernel sets an error flag
+// that the host reads at its next synchronisation, drains its copies in flight and returns.
 #include "k3moe_internal.cuh"
 
 namespace k3 {
 namespace {
+
+// ------------------------------------------------------------------- PTX helpers ---
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long now_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait on one phase of an mbarrier.  false: the wait gave up (error flag set) or
+// another thread of the grid already reported an error.
+__device__ __noinline__ bool wait_phase(uint64_t* bar, uint32_t parity, uint32_t* err, unsigned long long limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = now_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0u) {
+      if (*reinterpret_cast<volatile uint32_t*>(err) != 0u) return false;
+      if (now_ns() - t0 > limit_ns) {
+        atomicOr(err, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
+__device__ __forceinline__ uint2 lds64(const uint8_t* p) { return *reinterpret_cast<const uint2*>(p); }
 
 __device__ __forceinline__ void dec4(uint32_t w, uint32_t (&a)[4]) {
   asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t"
@@ -49,32 +122,11 @@ __device__ __forceinline__ void mma_zero(float (&d)[4], const uint32_t (&a)[4], 
 // E8M0 byte -> 2^(s-127) as fp32 (s = 0 is the subnormal 2^-127).
 __device__ __forceinline__ float e8m0f(uint32_t s) { return __uint_as_float(s ? (s << 23) : 0x00400000u); }
 
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t p;
-  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
-__device__ __forceinline__ uint4 ld_stream16(const uint8_t* ptr, uint64_t pol) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(ptr), "l"(pol));
-  return v;
-}
-
-__device__ __forceinline__ uint2 ld_stream8(const uint8_t* ptr, uint64_t pol) {
-  uint2 v;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v2.u32 {%0,%1}, [%2], %3;"
-               : "=r"(v.x), "=r"(v.y)
-               : "l"(ptr), "l"(pol));
-  return v;
-}
-
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int s) {
   return s == 0 ? v.x : (s == 1 ? v.y : (s == 2 ? v.z : v.w));
 }
 
+// power-of-two exponent q with m * 2^-q in [2^14, 2^15): the fp16 image never overflows
 __device__ __forceinline__ int fp16_scale_exp(float m) {
   if (!(m > 0.0f)) return 0;
   const int ex = (int)((__float_as_uint(m) >> 23) & 0xFFu) - 127;
@@ -83,302 +135,579 @@ __device__ __forceinline__ int fp16_scale_exp(float m) {
 }
 __device__ __forceinline__ float exp2i(int q) { return __uint_as_float((uint32_t)(127 + q) << 23); }
 
-constexpr int kWarps = 8;
+constexpr int kConsumers = 8;
+constexpr int kStageAlign = 128;
+constexpr int kMaxDepth = 6;  // outstanding cp.async groups per thread
+
+// Asynchronous 16-byte global -> shared copy (L2 only).  The policy argument is unused: the
+// copies go through L2 with the default eviction priority.
+#ifdef K3MOE_DEVICE_CHECKS
+// Self-checking build: a misaligned or out-of-ring copy records kErrBadAccess and is skipped.
+// Bounds are per CTA (shared-window offsets), set by thread 0 before the first copy.
+__shared__ uint32_t g_chk_lo, g_chk_hi;
+__shared__ uint32_t* g_chk_err;
+#endif
+__device__ __forceinline__ void cp16(void* dst, const void* src, uint64_t pol) {
+  (void)pol;
+#ifdef K3MOE_DEVICE_CHECKS
+  const uint32_t d = smem_u32(dst);
+  if ((d & 15u) != 0u || ((uintptr_t)src & 15u) != 0u || d < g_chk_lo || d + 16u > g_chk_hi) {
+    atomicOr(g_chk_err, kErrBadAccess);
+    return;
+  }
+#endif
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void cp_wait_dyn(int n) {
+  // wait until at most n (< kMaxDepth) of this thread's copy groups are pending
+  switch (n) {
+    case 0: cp_wait<0>(); break;
+    case 1: cp_wait<1>(); break;
+    case 2: cp_wait<2>(); break;
+    case 3: cp_wait<3>(); break;
+    case 4: cp_wait<4>(); break;
+    default: cp_wait<5>(); break;
+  }
+}
+// the warp copies `bytes` (multiple of 16) from src to dst, 16 bytes per lane per step
+__device__ __forceinline__ void warp_copy(uint8_t* dst, const uint8_t* src, int bytes, int lane, uint64_t pol) {
+  for (int off = lane * 16; off < bytes; off += 512) cp16(dst + off, src + off, pol);
+}
+
+// One unit's descriptor spread over a warp: lane l < 36 holds 32-bit word l (lanes 0..31 only
+// hold words 0..31, which cover e, M, pick[8], tok[8], xs[8]; w[8] is words 28..35 and is read
+// through a second register).
+struct DescRegs {
+  int a;  // word lane
+  int b;  // word 32 + lane (lanes 0..3)
+};
+__device__ __forceinline__ DescRegs load_desc(const UnitDesc* U, int lane) {
+  const int* w = reinterpret_cast<const int*>(U);
+  DescRegs r;
+  r.a = __ldg(w + lane);
+  r.b = lane < 4 ? __ldg(w + 32 + lane) : 0;
+  return r;
+}
+__device__ __forceinline__ int d_e(const DescRegs& r) { return __shfl_sync(0xffffffffu, r.a, 0); }
+__device__ __forceinline__ int d_M(const DescRegs& r) { return __shfl_sync(0xffffffffu, r.a, 1); }
+__device__ __forceinline__ int d_pick(const DescRegs& r, int m) { return __shfl_sync(0xffffffffu, r.a, 4 + m); }
+__device__ __forceinline__ int d_tok(const DescRegs& r, int m) { return __shfl_sync(0xffffffffu, r.a, 12 + m); }
+__device__ __forceinline__ float d_w(const DescRegs& r, int m) {
+  // w[m] is word 28 + m: words 28..31 in .a, 32..35 in .b.  Both shuffles run on every lane
+  // (a full-mask shuffle must be executed by the whole warp), then each lane selects.
+  const int va = __shfl_sync(0xffffffffu, r.a, 28 + (m & 3));
+  const int vb = __shfl_sync(0xffffffffu, r.b, m & 3);
+  return __int_as_float(m < 4 ? va : vb);
+}
 
 // ------------------------------------------------------------------------ gate/up ---
-__global__ void __launch_bounds__(kWarps * 32, 2) gateup_kernel(FfnArgs a) {
-  __shared__ float red[kWarps][16][32];
-  __shared__ __half hstage[8][32];
-  __shared__ float s_hsc[8];
-  __shared__ float s_xs[8];
-  __shared__ int s_pick[8];
+// Each consumer warp streams its own stages (cp.async, `depth` stages ahead) into a private
+// ring, so nothing is shared on the data path.  Warp w owns k-tiles kt % 8 == w of every task.
+constexpr int kGuRed = 8;                            // partial-sum slots (multiple of kGuEpi)
+constexpr int kGuEpi = 4;                            // epilogue warps; task j -> warp j % kGuEpi
+constexpr int kGuThreads = (kConsumers + kGuEpi) * 32;
+constexpr int kGuTileBytes = 2 * kTileBytes;         // gate tile + up tile of one (row group, k-tile)
 
-  const int chunks = a.f / 32;
-  const int ai = blockIdx.x / chunks, c = blockIdx.x % chunks;
-  if (ai >= *a.ws.nact) return;
-  const int e = a.ws.act[ai];
-  const int M = a.ws.counts[e], pbase = a.ws.offsets[e];
-  const uint8_t* W = a.expert_ptr[e];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  const int ktiles = a.d / kTileCols;
-  const int kt0 = warp * ktiles / kWarps, kt1 = (warp + 1) * ktiles / kWarps;
-  const uint64_t pol = policy_evict_first();
+struct GuLayout {
+  int depth, stage_bytes;
+  size_t red_off, ring_off, total;
+};
 
-  for (int n0 = 0; n0 < M; n0 += 8) {
-    if (threadIdx.x < 8) {
-      const int n = n0 + threadIdx.x;
-      const int p = n < M ? a.ws.perm[pbase + n] : -1;
-      s_pick[threadIdx.x] = p;
-      s_xs[threadIdx.x] = p >= 0 ? a.ws.xscale[p / a.k] : 0.f;
+inline GuLayout gu_layout(int mcap, size_t budget) {
+  GuLayout L;
+  L.stage_bytes = (kGuTileBytes + mcap * 256 + kStageAlign - 1) / kStageAlign * kStageAlign;
+  L.red_off = 1024;  // barriers: 2*kGuRed + 1
+  L.ring_off = L.red_off + (size_t)kGuRed * kConsumers * 8 * 32 * sizeof(float);
+  int depth = (int)((budget - L.ring_off) / ((size_t)kConsumers * L.stage_bytes));
+  L.depth = depth > kMaxDepth ? kMaxDepth : depth;
+  L.total = L.ring_off + (size_t)kConsumers * L.depth * L.stage_bytes;
+  return L;
+}
+
+// k-tiles of warp w among the KT k-tiles of one task (kt % 8 == w)
+__device__ __forceinline__ int warp_kts(int KT, int w) { return w < KT ? (KT - w + kConsumers - 1) / kConsumers : 0; }
+
+__global__ void __launch_bounds__(kGuThreads, 1) gateup_kernel(FfnArgs a, GuLayout L) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* red_full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* red_empty = red_full + kGuRed;
+  uint64_t* never = red_empty + kGuRed;
+  float* red = reinterpret_cast<float*>(smem + L.red_off);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t* err = a.ws.sync + 1;
+
+#ifdef K3MOE_DEVICE_CHECKS
+  if (threadIdx.x == 0) {
+    g_chk_err = a.ws.sync + 1;
+    g_chk_lo = smem_u32(smem + L.ring_off);
+    g_chk_hi = smem_u32(smem + L.total);
+  }
+  __syncthreads();
+#endif
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kGuRed; ++i) {
+      mbar_init(&red_full[i], kConsumers);
+      mbar_init(&red_empty[i], 1);
     }
-    const bool has = n0 + g < M;
-    const int mypick = has ? a.ws.perm[pbase + n0 + g] : 0;
-    const uint4* xb = reinterpret_cast<const uint4*>(a.ws.xfrag + (size_t)(mypick / a.k) * a.d) + t;
+    mbar_init(never, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
 
-    float acc[2][2][4];
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-      for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) acc[i][j][q] = 0.f;
+  const int RG = a.f / kTileRows;  // row groups of gate/up
+  const int KT = a.d / kTileCols;  // k-tiles
+  const int ntasks = *a.ws.nunits * RG;
+  const size_t gu_stride = (size_t)KT * kGuTileBytes;  // bytes of one row group (gate+up, all k-tiles)
+  const int G = gridDim.x;
 
-    for (int kt = kt0; kt < kt1; ++kt) {
-      uint4 nib[2][2][2];
-      uint2 sc[2][2];
-#pragma unroll
-      for (int rg = 0; rg < 2; ++rg)
+  if (warp < kConsumers) {
+    // ------------------------------------------------------------------ consumers ---
+    const int g = lane >> 2, t = lane & 3;
+    uint8_t* ring = smem + L.ring_off + (size_t)warp * L.depth * L.stage_bytes;
+    const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_normal();
+    if (a.test_stall && !wait_phase(never, 0, err, a.wait_ns)) return;
+    const int cw = warp_kts(KT, warp);
+    const int my_tasks = blockIdx.x < ntasks ? (ntasks - blockIdx.x + G - 1) / G : 0;
+    const long long nstages = (long long)my_tasks * cw;
+
+    // issue cursor: task ji, k-tile index ci; descriptors of task ji and ji+1 (prefetched)
+    int ji = 0, ci = 0;
+    DescRegs dcur{0, 0}, dnext{0, 0};
+    const uint8_t* Wcur = nullptr;
+    if (my_tasks > 0) {
+      dcur = load_desc(a.ws.units + blockIdx.x / RG, lane);
+      if (my_tasks > 1) dnext = load_desc(a.ws.units + (blockIdx.x + G) / RG, lane);
+      Wcur = a.expert_ptr[d_e(dcur)] + (size_t)(blockIdx.x % RG) * gu_stride;
+    }
+    auto issue_next = [&](long long sidx) {
+      // copy stage sidx (= the issue cursor) into its ring slot, then advance the cursor
+      uint8_t* st = ring + (size_t)(sidx % L.depth) * L.stage_bytes;
+      const int kt = warp + kConsumers * ci;
+      warp_copy(st, Wcur + (size_t)kt * kGuTileBytes, kGuTileBytes, lane, pol_w);
+      const int M = d_M(dcur);
+      for (int m = 0; m < M; ++m)
+        warp_copy(st + kGuTileBytes + m * 256,
+                  reinterpret_cast<const uint8_t*>(a.ws.xfrag + (size_t)d_tok(dcur, m) * a.d + (size_t)kt * 128), 256,
+                  lane, pol_x);
+      if (++ci == cw) {
+        ci = 0;
+        ++ji;
+        dcur = dnext;
+        if (ji < my_tasks) Wcur = a.expert_ptr[d_e(dcur)] + (size_t)((blockIdx.x + ji * G) % RG) * gu_stride;
+        if (ji + 1 < my_tasks) dnext = load_desc(a.ws.units + (blockIdx.x + (ji + 1) * G) / RG, lane);
+      }
+    };
+    long long issued = 0;
+    for (; issued < nstages && issued < L.depth; ++issued) {
+      issue_next(issued);
+      cp_commit();
+    }
+
+    // every consume step commits one (possibly empty) group, so the group of the stage being
+    // consumed is always followed by exactly min(depth, nstages) - 1 newer groups
+    const int wait_n = (int)(nstages < L.depth ? nstages : L.depth) - 1;
+    long long consumed = 0;
+    int M_n = my_tasks > 0 ? __ldg(&a.ws.units[blockIdx.x / RG].M) : 0;
+    for (int j = 0; j < my_tasks; ++j) {
+      const int M = M_n;
+      if (j + 1 < my_tasks) M_n = __ldg(&a.ws.units[(blockIdx.x + (j + 1) * G) / RG].M);
+      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      for (int c = 0; c < cw; ++c, ++consumed) {
+        cp_wait_dyn(wait_n);
+        __syncwarp();
+        const uint8_t* st = ring + (size_t)(consumed % L.depth) * L.stage_bytes;
+        uint4 nib[2][2];
+        uint2 sc[2];
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
-          const uint8_t* tp = W + ((size_t)((2 * c + rg) * ktiles + kt) * 2 + m) * kTileBytes;
-          nib[rg][m][0] = ld_stream16(tp + lane * 16, pol);
-          nib[rg][m][1] = ld_stream16(tp + 512 + lane * 16, pol);
-          sc[rg][m] = ld_stream8(tp + kTileNibBytes + g * 8, pol);
+          nib[m][0] = lds128(st + m * kTileBytes + lane * 16);
+          nib[m][1] = lds128(st + m * kTileBytes + 512 + lane * 16);
+          sc[m] = lds64(st + m * kTileBytes + kTileNibBytes + g * 8);
         }
-      uint4 xv[4];
+        uint4 xv[4];
 #pragma unroll
-      for (int b = 0; b < 4; ++b) xv[b] = has ? __ldg(xb + (size_t)(4 * kt + b) * 4) : make_uint4(0, 0, 0, 0);
-
+        for (int b = 0; b < 4; ++b)
+          xv[b] = g < M ? lds128(st + kGuTileBytes + g * 256 + (b * 4 + t) * 16) : make_uint4(0, 0, 0, 0);
+        __syncwarp();
+        if (issued < nstages) {  // refill the slot just read
+          issue_next(issued);
+          ++issued;
+        }
+        cp_commit();
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const int u = b >> 1;
-        float bacc[2][2][4];
+        for (int b = 0; b < 4; ++b) {
+          float bacc[2][4];
 #pragma unroll
-        for (int st = 0; st < 2; ++st) {
-          const int s = 2 * (b & 1) + st;
-          const uint32_t b0 = st ? xv[b].z : xv[b].x, b1 = st ? xv[b].w : xv[b].y;
-#pragma unroll
-          for (int rg = 0; rg < 2; ++rg)
+          for (int st2 = 0; st2 < 2; ++st2) {
+            const int w = 2 * (b & 1) + st2;
+            const uint32_t b0 = st2 ? xv[b].z : xv[b].x, b1 = st2 ? xv[b].w : xv[b].y;
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
               uint32_t A[4];
-              dec4(word_of(nib[rg][m][u], s), A);
-              if (st == 0)
-                mma_zero(bacc[rg][m], A, b0, b1);
+              dec4(word_of(nib[m][b >> 1], w), A);
+              if (st2 == 0)
+                mma_zero(bacc[m], A, b0, b1);
               else
-                mma_acc(bacc[rg][m], A, b0, b1);
+                mma_acc(bacc[m], A, b0, b1);
             }
-        }
-#pragma unroll
-        for (int rg = 0; rg < 2; ++rg)
+          }
 #pragma unroll
           for (int m = 0; m < 2; ++m) {
-            const float s0 = e8m0f((sc[rg][m].x >> (8 * b)) & 0xFFu);
-            const float s8 = e8m0f((sc[rg][m].y >> (8 * b)) & 0xFFu);
-            acc[rg][m][0] = fmaf(bacc[rg][m][0], s0, acc[rg][m][0]);
-            acc[rg][m][1] = fmaf(bacc[rg][m][1], s0, acc[rg][m][1]);
-            acc[rg][m][2] = fmaf(bacc[rg][m][2], s8, acc[rg][m][2]);
-            acc[rg][m][3] = fmaf(bacc[rg][m][3], s8, acc[rg][m][3]);
+            const float s_lo = e8m0f((sc[m].x >> (8 * b)) & 0xFFu);
+            const float s_hi = e8m0f((sc[m].y >> (8 * b)) & 0xFFu);
+            acc[m][0] = fmaf(bacc[m][0], s_lo, acc[m][0]);
+            acc[m][1] = fmaf(bacc[m][1], s_lo, acc[m][1]);
+            acc[m][2] = fmaf(bacc[m][2], s_hi, acc[m][2]);
+            acc[m][3] = fmaf(bacc[m][3], s_hi, acc[m][3]);
           }
+        }
       }
-    }
-
-#pragma unroll
-    for (int rg = 0; rg < 2; ++rg)
+      const int r = j % kGuRed;
+      if (j >= kGuRed && !wait_phase(&red_empty[r], (uint32_t)((j / kGuRed - 1) & 1), err, a.wait_ns)) {
+        cp_wait<0>();
+        return;
+      }
+      float* rp = red + ((size_t)r * kConsumers + warp) * 8 * 32;
 #pragma unroll
       for (int m = 0; m < 2; ++m)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) red[warp][(rg * 2 + m) * 4 + q][lane] = acc[rg][m][q];
-    __syncthreads();
+        for (int q = 0; q < 4; ++q) rp[(m * 4 + q) * 32 + lane] = acc[m][q];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&red_full[r]);
+    }
+    cp_wait<0>();
+    return;
+  }
 
-    if (warp == 0) {
-      float hv[2][4];
-      float mx0 = 0.f, mx1 = 0.f;
+  // ------------------------------------------------------------------------ epilogue ---
+  {
+    const int ew = warp - kConsumers;  // 0..kGuEpi-1: tasks j with j % kGuEpi == ew
+    const int g = lane >> 2, t = lane & 3;
+    const int nblk = a.f / 32;
+    int j = ew;
+    int i = blockIdx.x + ew * G;
+    // lane m < 8 holds pick m and its x scale of the task's unit; prefetched a task ahead
+    int M_n = 0, pick_n = -1;
+    float xs_n = 0.f;
+    if (i < ntasks) {
+      const UnitDesc* U = a.ws.units + i / RG;
+      M_n = U->M;
+      pick_n = U->pick[lane & 7];
+      xs_n = U->xs[lane & 7];
+    }
+    for (; i < ntasks; i += kGuEpi * G, j += kGuEpi) {
+      const int M = M_n, mypick = pick_n;
+      const float myxs = xs_n;
+      const int inext = i + kGuEpi * G;
+      if (inext < ntasks) {
+        const UnitDesc* U = a.ws.units + inext / RG;
+        M_n = U->M;
+        pick_n = U->pick[lane & 7];
+        xs_n = U->xs[lane & 7];
+      }
+      const int r = j % kGuRed;
+      if (!wait_phase(&red_full[r], (uint32_t)((j / kGuRed) & 1), err, a.wait_ns)) return;
+      float v[8];
 #pragma unroll
-      for (int rg = 0; rg < 2; ++rg)
+      for (int q = 0; q < 8; ++q) {
+        float sum = 0.f;
+        for (int w = 0; w < kConsumers; ++w) sum += red[(((size_t)r * kConsumers + w) * 8 + q) * 32 + lane];
+        v[q] = sum;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&red_empty[r]);
+
+      const int rg = i % RG;
+      const int blk = rg >> 1;
+      // SwiGLU for this lane's entries: rows 16rg+g (+8), columns (picks) 2t, 2t+1
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float gs = 0.f, us = 0.f;
-          for (int w = 0; w < kWarps; ++w) {
-            gs += red[w][(rg * 2 + 0) * 4 + q][lane];
-            us += red[w][(rg * 2 + 1) * 4 + q][lane];
+      for (int c = 0; c < 2; ++c) {
+        const int n = 2 * t + c;
+        const int p = __shfl_sync(0xffffffffu, mypick, n);
+        const float xs = __shfl_sync(0xffffffffu, myxs, n);
+        if (n < M) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float gv = v[0 * 4 + 2 * h + c] * xs, uv = v[1 * 4 + 2 * h + c] * xs;
+            const float hv = gv / (1.0f + expf(-gv)) * uv;
+            a.ws.hbuf[(size_t)p * a.f + rg * kTileRows + g + 8 * h] = hv;
           }
-          const float xs = s_xs[2 * t + (q & 1)];
-          const float gt = gs * xs, ut = us * xs;
-          const float h = gt / (1.0f + expf(-gt)) * ut;
-          hv[rg][q] = h;
-          if (q & 1)
-            mx1 = fmaxf(mx1, fabsf(h));
-          else
-            mx0 = fmaxf(mx0, fabsf(h));
-        }
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-      }
-      const int q0 = fp16_scale_exp(mx0), q1 = fp16_scale_exp(mx1);
-      const float i0 = exp2i(-q0), i1 = exp2i(-q1);
-#pragma unroll
-      for (int rg = 0; rg < 2; ++rg)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int r = 16 * rg + g + 8 * (q >> 1);
-          const int n = 2 * t + (q & 1);
-          hstage[n][r] = __float2half_rn(hv[rg][q] * ((q & 1) ? i1 : i0));
-        }
-      if (g == 0) {
-        s_hsc[2 * t] = exp2i(q0);
-        s_hsc[2 * t + 1] = exp2i(q1);
-      }
-    }
-    __syncthreads();
-    if (threadIdx.x < 32) {
-      const int n = threadIdx.x >> 2, tq = threadIdx.x & 3;
-      const int p = s_pick[n];
-      if (p >= 0) {
-        __align__(16) __half hh[8];
-#pragma unroll
-        for (int s = 0; s < 2; ++s) {
-          hh[4 * s + 0] = hstage[n][16 * s + 2 * tq];
-          hh[4 * s + 1] = hstage[n][16 * s + 2 * tq + 1];
-          hh[4 * s + 2] = hstage[n][16 * s + 2 * tq + 8];
-          hh[4 * s + 3] = hstage[n][16 * s + 2 * tq + 9];
-        }
-        *reinterpret_cast<uint4*>(a.ws.hfrag + (size_t)p * a.f + (size_t)(c * 4 + tq) * 8) =
-            *reinterpret_cast<const uint4*>(hh);
-        if (tq == 0) a.ws.hscale[(size_t)p * chunks + c] = s_hsc[n];
-      }
-    }
-    __syncthreads();
-  }
-}
-
-// --------------------------------------------------------------------- down+combine ---
-__global__ void __launch_bounds__(kWarps * 32, 2) down_kernel(FfnArgs a) {
-  __shared__ float red[4][4][32];
-  __shared__ int s_pick[8];
-  __shared__ float s_w[8];
-  __shared__ int s_last[8];
-
-  const int chunks = a.d / 64;
-  const int ai = blockIdx.x / chunks, c = blockIdx.x % chunks;
-  if (ai >= *a.ws.nact) return;
-  const int e = a.ws.act[ai];
-  const int M = a.ws.counts[e], pbase = a.ws.offsets[e];
-  const uint8_t* W = a.expert_ptr[e] + gateup_region_bytes(a.d, a.f);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  const int rgl = warp & 3, half = warp >> 2;
-  const int rg = 4 * c + rgl;
-  const int ktiles = a.f / kTileCols;
-  const int nblk = a.f / 32;
-  int kt0, kt1;
-  if (ktiles >= 2) {
-    kt0 = half * ktiles / 2;
-    kt1 = (half + 1) * ktiles / 2;
-  } else {
-    kt0 = 0;
-    kt1 = half == 0 ? ktiles : 0;
-  }
-  const uint64_t pol = policy_evict_first();
-
-  for (int n0 = 0; n0 < M; n0 += 8) {
-    if (threadIdx.x < 8) {
-      const int n = n0 + threadIdx.x;
-      const int p = n < M ? a.ws.perm[pbase + n] : -1;
-      s_pick[threadIdx.x] = p;
-      s_w[threadIdx.x] = p >= 0 ? a.ws.w[p] : 0.f;
-    }
-    __syncthreads();
-    const bool has = n0 + g < M;
-    const int mypick = has ? s_pick[g] : 0;
-    const uint4* hb = reinterpret_cast<const uint4*>(a.ws.hfrag + (size_t)mypick * a.f) + t;
-    const int p0 = s_pick[2 * t], p1 = s_pick[2 * t + 1];
-    const float* hs0 = a.ws.hscale + (size_t)(p0 >= 0 ? p0 : 0) * nblk;
-    const float* hs1 = a.ws.hscale + (size_t)(p1 >= 0 ? p1 : 0) * nblk;
-
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int kt = kt0; kt < kt1; ++kt) {
-      const uint8_t* tp = W + ((size_t)rg * ktiles + kt) * kTileBytes;
-      const uint4 n_0 = ld_stream16(tp + lane * 16, pol);
-      const uint4 n_1 = ld_stream16(tp + 512 + lane * 16, pol);
-      const uint2 sc = ld_stream8(tp + kTileNibBytes + g * 8, pol);
-      uint4 hv[4];
-#pragma unroll
-      for (int b = 0; b < 4; ++b) hv[b] = has ? __ldg(hb + (size_t)(4 * kt + b) * 4) : make_uint4(0, 0, 0, 0);
-      float h0[4], h1[4];
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        h0[b] = p0 >= 0 ? __ldg(hs0 + 4 * kt + b) : 0.f;
-        h1[b] = p1 >= 0 ? __ldg(hs1 + 4 * kt + b) : 0.f;
-      }
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const uint4& nv = (b >> 1) ? n_1 : n_0;
-        float bacc[4];
-#pragma unroll
-        for (int st = 0; st < 2; ++st) {
-          const int s = 2 * (b & 1) + st;
-          uint32_t A[4];
-          dec4(word_of(nv, s), A);
-          const uint32_t b0 = st ? hv[b].z : hv[b].x, b1 = st ? hv[b].w : hv[b].y;
-          if (st == 0)
-            mma_zero(bacc, A, b0, b1);
-          else
-            mma_acc(bacc, A, b0, b1);
-        }
-        const float s0 = e8m0f((sc.x >> (8 * b)) & 0xFFu);
-        const float s8 = e8m0f((sc.y >> (8 * b)) & 0xFFu);
-        acc[0] = fmaf(bacc[0], s0 * h0[b], acc[0]);
-        acc[1] = fmaf(bacc[1], s0 * h1[b], acc[1]);
-        acc[2] = fmaf(bacc[2], s8 * h0[b], acc[2]);
-        acc[3] = fmaf(bacc[3], s8 * h1[b], acc[3]);
-      }
-    }
-    if (half == 1) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) red[rgl][q][lane] = acc[q];
-    }
-    __syncthreads();
-    if (half == 0) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float o = acc[q] + red[rgl][q][lane];
-        const int n = 2 * t + (q & 1);
-        const int p = s_pick[n];
-        if (p >= 0) {
-          const int row = 64 * c + 16 * rgl + g + 8 * (q >> 1);
-          a.ws.obuf[(size_t)p * a.d + row] = o * s_w[n];
         }
       }
-      __threadfence();
-    }
-    __syncthreads();
-    if (threadIdx.x < 8) {
-      const int p = s_pick[threadIdx.x];
+      __syncwarp();
+      // the second of the two 16-row halves of a 32-row block converts it, per pick: lane m's
+      // acq_rel increment publishes this warp's h rows and, on the second arrival, makes the
+      // other half's rows visible
       int last = 0;
-      if (p >= 0) {
-        const int tok = p / a.k;
-        last = atomicAdd(&a.ws.arrive[(size_t)tok * chunks + c], 1) == a.k - 1;
+      if (lane < M) {
+        int old;
+        asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;"
+                     : "=r"(old)
+                     : "l"(a.ws.pair + (size_t)mypick * nblk + blk)
+                     : "memory");
+        last = old == 1;
       }
-      s_last[threadIdx.x] = last;
-    }
-    __syncthreads();
-    for (int n = 0; n < 8; ++n) {
-      if (!s_last[n]) continue;
-      __threadfence();
-      const int tok = s_pick[n] / a.k;
-      if (threadIdx.x < 64) {
-        const int row = 64 * c + threadIdx.x;
-        float y = 0.f;
-        for (int slot = 0; slot < a.k; ++slot) y += __ldcg(a.ws.obuf + ((size_t)tok * a.k + slot) * a.d + row);
-        a.y[(size_t)tok * a.d + row] = y;
+      unsigned todo = __ballot_sync(0xffffffffu, last);
+      while (todo) {
+        const int m = __ffs(todo) - 1;
+        todo &= todo - 1;
+        const int p = __shfl_sync(0xffffffffu, mypick, m);
+        const float hv = __ldcg(a.ws.hbuf + (size_t)p * a.f + blk * 32 + lane);
+        float mx = fabsf(hv);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const int q = fp16_scale_exp(mx);
+        const uint16_t hb = __half_as_ushort(__float2half_rn(hv * exp2i(-q)));
+        // lane tq < 4 gathers rows 16s + 2tq + {0, 1, 8, 9} (s = 0, 1) of the block
+        __align__(16) uint16_t frag[8];
+#pragma unroll
+        for (int s2 = 0; s2 < 2; ++s2) {
+          const int base = 16 * s2 + 2 * (lane & 3);
+          frag[4 * s2 + 0] = (uint16_t)__shfl_sync(0xffffffffu, (int)hb, base);
+          frag[4 * s2 + 1] = (uint16_t)__shfl_sync(0xffffffffu, (int)hb, base + 1);
+          frag[4 * s2 + 2] = (uint16_t)__shfl_sync(0xffffffffu, (int)hb, base + 8);
+          frag[4 * s2 + 3] = (uint16_t)__shfl_sync(0xffffffffu, (int)hb, base + 9);
+        }
+        if (lane < 4)
+          *reinterpret_cast<uint4*>(a.ws.hfrag + (size_t)p * a.f + (size_t)(blk * 4 + lane) * 8) =
+              *reinterpret_cast<const uint4*>(frag);
+        if (lane == 0) {
+          a.ws.hscale[(size_t)p * nblk + blk] = exp2i(q);
+          a.ws.pair[(size_t)p * nblk + blk] = 0;
+        }
       }
-      if (threadIdx.x == 0) a.ws.arrive[(size_t)tok * chunks + c] = 0;
     }
-    __syncthreads();
   }
 }
+
+// --------------------------------------------------------------------------- down ---
+// Task = (unit, 16 rows of d) over the whole f range; warp w owns the CTA's tasks j % 8 == w and
+// streams each task in chunks of kc k-tiles (one ring stage per chunk) into a private ring.
+constexpr int kDnThreads = kConsumers * 32;
+
+struct DnLayout {
+  int depth, kc, nch, stage_bytes;
+  size_t total;
+};
+
+inline DnLayout dn_layout(int f, int mcap, size_t budget) {
+  DnLayout L;
+  const int KT = f / kTileCols;
+  const size_t per_kt = kTileBytes + (size_t)mcap * (4 * 64 + 4 * 4);  // weights + h fragments + h scales
+  int kc = (int)(budget / ((size_t)kConsumers * 3 * per_kt));           // aim for 3 stages per warp
+  kc = kc < 1 ? 1 : (kc > KT ? KT : kc);
+  L.kc = kc;
+  L.nch = (KT + kc - 1) / kc;
+  L.stage_bytes = (int)((kc * per_kt + kStageAlign - 1) / kStageAlign * kStageAlign);
+  int depth = (int)(budget / ((size_t)kConsumers * L.stage_bytes));
+  L.depth = depth > kMaxDepth ? kMaxDepth : depth;
+  L.total = (size_t)kConsumers * L.depth * L.stage_bytes;
+  return L;
+}
+
+__global__ void __launch_bounds__(kDnThreads, 1) down_kernel(FfnArgs a, DnLayout L) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  uint32_t* err = a.ws.sync + 1;
+  if (a.test_stall) {  // failure-path test: wait on a barrier that nothing completes
+    __shared__ uint64_t never;
+    if (threadIdx.x == 0) {
+      mbar_init(&never, 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (!wait_phase(&never, 0, err, a.wait_ns)) return;
+  }
+
+#ifdef K3MOE_DEVICE_CHECKS
+  if (threadIdx.x == 0) {
+    g_chk_err = a.ws.sync + 1;
+    g_chk_lo = smem_u32(smem);
+    g_chk_hi = smem_u32(smem + L.total);
+  }
+  __syncthreads();
+#endif
+  const int RG = a.d / kTileRows;
+  const int KT = a.f / kTileCols;
+  const int ntasks = *a.ws.nunits * RG;
+  const size_t gu_bytes = gateup_region_bytes(a.d, a.f);
+  const int nblk = a.f / 32;
+  const int wb = L.kc * kTileBytes;  // weight bytes of a full chunk
+  const int G = gridDim.x;
+  // stage: [kc weight tiles][M x kc*256 h fragments][M x kc*16 h scales]
+  uint8_t* ring = smem + (size_t)warp * L.depth * L.stage_bytes;
+  const uint64_t pol_w = policy_evict_first(), pol_h = policy_evict_normal();
+  const int first = blockIdx.x + warp * G, step = kConsumers * G;
+  const int my_tasks = first < ntasks ? (ntasks - first + step - 1) / step : 0;
+  const long long nstages = (long long)my_tasks * L.nch;
+
+  int ji = 0, ci = 0;
+  DescRegs dcur{0, 0}, dnext{0, 0};
+  const uint8_t* Wcur = nullptr;
+  if (my_tasks > 0) {
+    dcur = load_desc(a.ws.units + first / RG, lane);
+    if (my_tasks > 1) dnext = load_desc(a.ws.units + (first + step) / RG, lane);
+    Wcur = a.expert_ptr[d_e(dcur)] + gu_bytes + (size_t)(first % RG) * KT * kTileBytes;
+  }
+  auto issue_next = [&](long long sidx) {
+    uint8_t* st = ring + (size_t)(sidx % L.depth) * L.stage_bytes;
+    const int kt0 = ci * L.kc, nk = min(L.kc, KT - kt0);
+    warp_copy(st, Wcur + (size_t)kt0 * kTileBytes, nk * kTileBytes, lane, pol_w);
+    const int M = d_M(dcur);
+    for (int m = 0; m < M; ++m) {
+      const int p = d_pick(dcur, m);
+      warp_copy(st + wb + m * L.kc * 256, reinterpret_cast<const uint8_t*>(a.ws.hfrag + (size_t)p * a.f) + kt0 * 256,
+                nk * 256, lane, pol_h);
+      warp_copy(st + wb + M * L.kc * 256 + m * L.kc * 16,
+                reinterpret_cast<const uint8_t*>(a.ws.hscale + (size_t)p * nblk) + kt0 * 16, nk * 16, lane, pol_h);
+    }
+    if (++ci == L.nch) {
+      ci = 0;
+      ++ji;
+      dcur = dnext;
+      if (ji < my_tasks)
+        Wcur = a.expert_ptr[d_e(dcur)] + gu_bytes + (size_t)((first + ji * step) % RG) * KT * kTileBytes;
+      if (ji + 1 < my_tasks) dnext = load_desc(a.ws.units + (first + (ji + 1) * step) / RG, lane);
+    }
+  };
+  long long issued = 0;
+  for (; issued < nstages && issued < L.depth; ++issued) {
+    issue_next(issued);
+    cp_commit();
+  }
+
+  const int wait_n = (int)(nstages < L.depth ? nstages : L.depth) - 1;
+  long long consumed = 0;
+  DescRegs dtask = my_tasks > 0 ? load_desc(a.ws.units + first / RG, lane) : DescRegs{0, 0};
+  for (int j = 0; j < my_tasks; ++j) {
+    const int i = first + j * step;
+    const DescRegs D = dtask;
+    if (j + 1 < my_tasks) dtask = load_desc(a.ws.units + (i + step) / RG, lane);
+    const int M = d_M(D);
+    const int rg = i % RG;
+    const int n0 = 2 * t, n1 = 2 * t + 1;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int c = 0; c < L.nch; ++c, ++consumed) {
+      cp_wait_dyn(wait_n);
+      __syncwarp();
+      const uint8_t* st = ring + (size_t)(consumed % L.depth) * L.stage_bytes;
+      const uint8_t* hrow = st + wb + g * L.kc * 256;
+      const float* hs = reinterpret_cast<const float*>(st + wb + M * L.kc * 256);
+      const float* hs0 = hs + (n0 < M ? n0 : 0) * L.kc * 4;
+      const float* hs1 = hs + (n1 < M ? n1 : 0) * L.kc * 4;
+      const int nk = min(L.kc, KT - c * L.kc);
+      for (int kk = 0; kk < nk; ++kk) {
+        const uint8_t* tp = st + (size_t)kk * kTileBytes;
+        const uint4 u0 = lds128(tp + lane * 16), u1 = lds128(tp + 512 + lane * 16);
+        const uint2 sc = lds64(tp + kTileNibBytes + g * 8);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const uint4 hv = g < M ? lds128(hrow + (size_t)(4 * kk + b) * 64 + t * 16) : make_uint4(0, 0, 0, 0);
+          const uint4& nv = (b >> 1) ? u1 : u0;
+          float bacc[4];
+          uint32_t A[4];
+          dec4(word_of(nv, 2 * (b & 1)), A);
+          mma_zero(bacc, A, hv.x, hv.y);
+          dec4(word_of(nv, 2 * (b & 1) + 1), A);
+          mma_acc(bacc, A, hv.z, hv.w);
+          const float s_lo = e8m0f((sc.x >> (8 * b)) & 0xFFu);
+          const float s_hi = e8m0f((sc.y >> (8 * b)) & 0xFFu);
+          const float h0 = n0 < M ? hs0[4 * kk + b] : 0.f;
+          const float h1 = n1 < M ? hs1[4 * kk + b] : 0.f;
+          acc[0] = fmaf(bacc[0], s_lo * h0, acc[0]);
+          acc[1] = fmaf(bacc[1], s_lo * h1, acc[1]);
+          acc[2] = fmaf(bacc[2], s_hi * h0, acc[2]);
+          acc[3] = fmaf(bacc[3], s_hi * h1, acc[3]);
+        }
+      }
+      __syncwarp();
+      if (issued < nstages) {
+        issue_next(issued);
+        ++issued;
+      }
+      cp_commit();
+    }
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int n = 2 * t + c;
+      const int p = d_pick(D, n);
+      const float wp = d_w(D, n);
+      if (n < M) {
+        a.ws.obuf[(size_t)p * a.d + rg * kTileRows + g] = acc[c] * wp;
+        a.ws.obuf[(size_t)p * a.d + rg * kTileRows + g + 8] = acc[2 + c] * wp;
+      }
+    }
+  }
+  cp_wait<0>();
+}
+
+// ------------------------------------------------------------------------- combine ---
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ obuf, int T, int d, int k,
+                                                      float* __restrict__ y) {
+  const size_t n4 = (size_t)T * d / 4;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t t = i / (d / 4), c4 = i % (d / 4);
+    const float4* src = reinterpret_cast<const float4*>(obuf + (size_t)t * k * d) + c4;
+    float4 acc = __ldg(src);
+    for (int slot = 1; slot < k; ++slot) {
+      const float4 v = __ldg(src + (size_t)slot * (d / 4));
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    reinterpret_cast<float4*>(y)[i] = acc;
+  }
+}
+
+constexpr size_t kSmemBudget = 220 * 1024;
 
 }  // namespace
 
 cudaError_t launch_gateup(const FfnArgs& a, cudaStream_t s) {
-  gateup_kernel<<<a.max_tasks * (a.f / 32), kWarps * 32, 0, s>>>(a);
+  const int mcap = a.T < kUnitTokens ? a.T : kUnitTokens;
+  GuLayout L = gu_layout(mcap, kSmemBudget);
+  if (a.ring_depth > 0 && a.ring_depth < L.depth) {
+    L.depth = a.ring_depth;
+    L.total = L.ring_off + (size_t)kConsumers * L.depth * L.stage_bytes;
+  }
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  gateup_kernel<<<a.num_sms, kGuThreads, L.total, s>>>(a, L);
   return cudaGetLastError();
 }
 
 cudaError_t launch_down(const FfnArgs& a, cudaStream_t s) {
-  down_kernel<<<a.max_tasks * (a.d / 64), kWarps * 32, 0, s>>>(a);
+  const int mcap = a.T < kUnitTokens ? a.T : kUnitTokens;
+  DnLayout L = dn_layout(a.f, mcap, kSmemBudget);
+  if (a.ring_depth > 0 && a.ring_depth < L.depth) {
+    L.depth = a.ring_depth;
+    L.total = (size_t)kConsumers * L.depth * L.stage_bytes;
+  }
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  down_kernel<<<a.num_sms, kDnThreads, L.total, s>>>(a, L);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const FfnArgs& a, cudaStream_t s) {
+  const size_t n4 = (size_t)a.T * a.d / 4;
+  const int grid = (int)std::min<size_t>((n4 + 255) / 256, (size_t)a.num_sms * 8);
+  combine_kernel<<<grid, 256, 0, s>>>(a.ws.obuf, a.T, a.d, a.k, a.y);
   return cudaGetLastError();
 }
 

@@ -47,6 +47,22 @@ __host__ __device__ inline size_t gateup_region_bytes(int d, int f) { return (si
 //   i.e. registers b0b1, b2b3 of step 0 then of step 1, as mma.m16n8k16 expects for column n.
 // Row stride = K * 2 bytes.
 
+// A work unit is (expert, up to kUnitTokens consecutive picks of that expert): the FFN kernels
+// multiply one unit's tokens as the n = 8 columns of mma.m16n8k16.  Bucketing writes one flat
+// descriptor per unit so that the FFN kernels fetch everything about a unit in one go.
+constexpr int kUnitTokens = 8;
+struct __align__(16) UnitDesc {
+  int e;                    // expert id
+  int M;                    // picks in the unit (1..8)
+  int pbase;                // index of the unit's first pick in perm
+  int pad;
+  int pick[kUnitTokens];    // pick ids p = t*k + slot
+  int tok[kUnitTokens];     // token ids t
+  float xs[kUnitTokens];    // power-of-two scale of the token's fp16 image
+  float w[kUnitTokens];     // combine weight of the pick
+};
+static_assert(sizeof(UnitDesc) == 144, "UnitDesc is 9 x 16 bytes");
+
 // Workspace of one layer, sized for T_max tokens (P = T_max*k picks).
 struct Workspace {
   float* logits = nullptr;      // [T_max][E]
@@ -59,11 +75,14 @@ struct Workspace {
   int32_t* perm = nullptr;      // [P]
   int32_t* act = nullptr;       // [E] active experts in id order
   int32_t* nact = nullptr;      // [1]
+  UnitDesc* units = nullptr;    // [P/8 + E] work units
+  int32_t* nunits = nullptr;    // [1]
+  float* hbuf = nullptr;        // [P][f] SwiGLU output, fp32
+  int32_t* pair = nullptr;      // [P][f/32] halves of a 32-row block written (kept at zero between calls)
   __half* hfrag = nullptr;      // [P][f] fragment order
   float* hscale = nullptr;      // [P][f/32] power of two per (pick, 32-block)
   float* obuf = nullptr;        // [P][d] w-scaled expert outputs
-  int32_t* arrive = nullptr;    // [T_max][d/64] combine arrival counters (kept at zero)
-  uint32_t* sync = nullptr;     // [8] grid counters (router last-block) + error flags
+  uint32_t* sync = nullptr;     // [16]: [0] router last-block ticket, [1] device error flags
   int32_t* bad = nullptr;       // [1] pack-time error flag
 };
 
@@ -92,17 +111,26 @@ cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* idx, float* w,
                         cudaStream_t s);
 cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* counts, int32_t* offsets,
-                          int32_t* perm, int32_t* act, int32_t* nact, cudaStream_t s);
+                          int32_t* perm, int32_t* act, int32_t* nact, UnitDesc* units, int32_t* nunits,
+                          const float* w, const float* xscale, cudaStream_t s);
+
+// Device error flags (ws.sync[1]).
+constexpr uint32_t kErrTimeout = 1u;
+constexpr uint32_t kErrBadAccess = 2u;  // self-checking builds only: a copy address failed its check
 
 struct FfnArgs {
   const uint8_t* const* expert_ptr;  // [E] device pointers to each expert's packed block
   int d, f, E, k, T;
   Workspace ws;
   float* y;                          // [T][d]
-  int max_tasks;                     // grid size bound (active experts are not known on the host)
+  int num_sms;                       // persistent grid size
+  unsigned long long wait_ns;        // bound on every device-side wait
+  int test_stall;                    // 1: consumers wait on a barrier nothing arrives at (timeout test)
+  int ring_depth;                    // 0: automatic; else stages in flight per streaming warp
 };
 cudaError_t launch_gateup(const FfnArgs& a, cudaStream_t s);
 cudaError_t launch_down(const FfnArgs& a, cudaStream_t s);
+cudaError_t launch_combine(const FfnArgs& a, cudaStream_t s);
 
 // canon_nib/canon_scl point at the canonical bytes of the first of n_exp experts; dst at its packed block.
 cudaError_t launch_pack(const uint8_t* canon_nib, const uint8_t* canon_scl, int n_exp, int d, int f, uint8_t* dst,

@@ -46,6 +46,7 @@ __device__ void logits_rows(const RouterArgs& a) {
   for (int t0 = 0; t0 < a.T; t0 += kTokTile) {
     float acc[kTokTile] = {0.f, 0.f, 0.f, 0.f};
     const int nt = min(kTokTile, a.T - t0);
+#pragma unroll 8
     for (int q = lane; q < nq; q += 32) {
       const float4 w = __ldg(wr + q);
 #pragma unroll
@@ -146,8 +147,10 @@ __device__ void topk_warp(const float* logits_row, const float* bias, int E, int
 
 // ------------------------------------------------------------------------ bucketing ---
 // Whole-block deterministic bucketing of P picks.  smem: 2*E ints.
-__device__ void bucket_block(const int32_t* idx, int P, int E, int32_t* counts, int32_t* offsets, int32_t* perm,
-                             int32_t* act, int32_t* nact, int* smem) {
+__device__ void bucket_block(const int32_t* idx, int P, int k, int E, int32_t* counts, int32_t* offsets,
+                             int32_t* perm, int32_t* act, int32_t* nact, UnitDesc* units, int32_t* nunits,
+                             const float* w, const float* xscale, int* smem) {
+  __shared__ int s_nunits;
   int* cnt = smem;
   int* cur = smem + E;
   const int tid = threadIdx.x, bd = blockDim.x, warp = tid >> 5, lane = tid & 31, nwarps = bd >> 5;
@@ -159,15 +162,20 @@ __device__ void bucket_block(const int32_t* idx, int P, int E, int32_t* counts, 
   }
   __syncthreads();
   if (warp == 0) {
-    int run = 0, arun = 0;
+    int run = 0, arun = 0, urun = 0;
     for (int base = 0; base < E; base += 32) {
       const int e = base + lane;
       const int v = e < E ? cnt[e] : 0;
-      int inc = v;
+      const int np = (v + kUnitTokens - 1) / kUnitTokens;  // work units of <= 8 picks
+      int inc = v, uinc = np;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const int o = __shfl_up_sync(0xffffffffu, inc, off);
-        if (lane >= off) inc += o;
+        const int uo = __shfl_up_sync(0xffffffffu, uinc, off);
+        if (lane >= off) {
+          inc += o;
+          uinc += uo;
+        }
       }
       const unsigned nz = __ballot_sync(0xffffffffu, v > 0);
       if (e < E) {
@@ -175,13 +183,23 @@ __device__ void bucket_block(const int32_t* idx, int P, int E, int32_t* counts, 
         offsets[e] = run + inc - v;
         counts[e] = v;
         if (v > 0) act[arun + __popc(nz & ((1u << lane) - 1u))] = e;
+        for (int i = 0; i < np; ++i) {
+          UnitDesc& U = units[urun + uinc - np + i];
+          U.e = e;
+          U.M = min(kUnitTokens, v - i * kUnitTokens);
+          U.pbase = run + inc - v + i * kUnitTokens;
+          U.pad = 0;
+        }
       }
       run += __shfl_sync(0xffffffffu, inc, 31);
+      urun += __shfl_sync(0xffffffffu, uinc, 31);
       arun += __popc(nz);
     }
     if (lane == 0) {
       offsets[E] = run;
       *nact = arun;
+      *nunits = urun;
+      s_nunits = urun;
     }
   }
   __syncthreads();
@@ -203,6 +221,21 @@ __device__ void bucket_block(const int32_t* idx, int P, int E, int32_t* counts, 
         }
       }
       __syncthreads();
+    }
+  }
+  // per-unit pick lists (perm was written by this block above)
+  __threadfence_block();
+  __syncthreads();
+  for (int u = tid; u < s_nunits; u += bd) {
+    UnitDesc& U = units[u];
+    const int M = U.M, pb = U.pbase;
+    for (int m = 0; m < kUnitTokens; ++m) {
+      const int p = m < M ? __ldcg(perm + pb + m) : 0;
+      const int t = p / k;
+      U.pick[m] = m < M ? p : -1;
+      U.tok[m] = m < M ? t : 0;
+      U.xs[m] = m < M ? __ldcg(xscale + t) : 0.f;
+      U.w[m] = m < M ? __ldcg(w + p) : 0.f;
     }
   }
 }
@@ -228,8 +261,8 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(RouterArgs a)
               a.ws.w + (size_t)t * a.k);
   __threadfence_block();
   __syncthreads();
-  bucket_block(a.ws.idx, a.T * a.k, a.E, a.ws.counts, a.ws.offsets, a.ws.perm, a.ws.act, a.ws.nact,
-               reinterpret_cast<int*>(dsm));
+  bucket_block(a.ws.idx, a.T * a.k, a.k, a.E, a.ws.counts, a.ws.offsets, a.ws.perm, a.ws.act, a.ws.nact,
+               a.ws.units, a.ws.nunits, a.ws.w, a.ws.xscale, reinterpret_cast<int*>(dsm));
   if (threadIdx.x == 0) a.ws.sync[0] = 0u;
 }
 
@@ -242,10 +275,12 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* logits, const fl
   topk_warp(logits + (size_t)t * E, bias, E, k, dsm + (size_t)warp * E, idx + (size_t)t * k, w + (size_t)t * k);
 }
 
-__global__ void __launch_bounds__(1024) bucket_kernel(const int32_t* idx, int P, int E, int32_t* counts,
-                                                      int32_t* offsets, int32_t* perm, int32_t* act, int32_t* nact) {
+__global__ void __launch_bounds__(1024) bucket_kernel(const int32_t* idx, int P, int k, int E, int32_t* counts,
+                                                      int32_t* offsets, int32_t* perm, int32_t* act, int32_t* nact,
+                                                      UnitDesc* units, int32_t* nunits, const float* w,
+                                                      const float* xscale) {
   extern __shared__ int ism[];
-  bucket_block(idx, P, E, counts, offsets, perm, act, nact, ism);
+  bucket_block(idx, P, k, E, counts, offsets, perm, act, nact, units, nunits, w, xscale, ism);
 }
 
 }  // namespace
@@ -274,13 +309,15 @@ cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, in
 }
 
 cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* counts, int32_t* offsets,
-                          int32_t* perm, int32_t* act, int32_t* nact, cudaStream_t s) {
+                          int32_t* perm, int32_t* act, int32_t* nact, UnitDesc* units, int32_t* nunits,
+                          const float* w, const float* xscale, cudaStream_t s) {
   static bool attr = false;
   if (!attr) {
     cudaFuncSetAttribute(bucket_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
     attr = true;
   }
-  bucket_kernel<<<1, 1024, (size_t)2 * E * sizeof(int), s>>>(idx, T * k, E, counts, offsets, perm, act, nact);
+  bucket_kernel<<<1, 1024, (size_t)2 * E * sizeof(int), s>>>(idx, T * k, k, E, counts, offsets, perm, act, nact,
+                                                              units, nunits, w, xscale);
   return cudaGetLastError();
 }
 

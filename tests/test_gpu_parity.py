@@ -293,3 +293,23 @@ def test_k3_batched_decode_t64(k3_layer):
     # whole-batch invariant at any size: bitwise repeatable
     _, _, y2 = _run(layer, x)
     assert np.array_equal(y, y2)
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    # A forward whose FFN consumers wait on a barrier that nothing completes: the bounded wait
+    # (50 ms here) gives up, the kernels return, k3moe_sync reports the timeout, and the next
+    # call on the same context is correct.  No GPU fault or hang is involved.
+    L = Small(256, 128, 8, 2, 4)
+    x = L.tokens(4)
+    y_ok = L.forward(x)
+    k3.k3moe_sync(L.layer)
+    k3.k3moe_set_option(L.layer, k3.K3MOE_OPT_DEVICE_WAIT_NS, 50_000_000)
+    k3.k3moe_set_option(L.layer, k3.K3MOE_OPT_TEST_STALL, 1)
+    y = torch.empty((4, 256), dtype=torch.float32, device="cuda")
+    k3.k3moe_layer_forward(L.layer, _dev(x), 4, y)
+    with pytest.raises(k3.K3MoEError) as ei:
+        k3.k3moe_sync(L.layer)
+    assert ei.value.code == k3.K3MOE_ERR_TIMEOUT
+    assert np.array_equal(L.forward(x), y_ok)
+    k3.k3moe_sync(L.layer)
+    L.free()
