@@ -106,6 +106,7 @@ struct k3moe_layer {
   unsigned long long wait_ns = 2000000000ull;  // bound on device-side waits
   int test_stall = 0;                           // next forward stalls its FFN consumers (timeout test)
   int ring_depth = 0;                           // 0: automatic
+  bool zero_scales = false;                     // some E8M0 scale byte is 0 (2^-127, a subnormal)
 };
 
 namespace {
@@ -224,7 +225,8 @@ bool use_gemm(const k3moe_layer* L, int T) {
 int run_routing(k3moe_layer* L, const void* x, int T, cudaStream_t s) {
   const k3moe_dims& D = L->dims;
   RouterArgs ra{reinterpret_cast<const uint16_t*>(x), L->Wr, L->bias, T, D.d, D.E, D.k, L->ws, 0};
-  ra.fuse_select = (T * D.k <= 1024) ? 1 : 0;
+  // the last router block selects serially token by token: worth it only for a few tokens
+  ra.fuse_select = (T <= 4 && T * D.k <= 1024) ? 1 : 0;
   int rc = timed_launch(L, KID_ROUTER, s, [&] { return launch_router(ra, s); });
   if (rc) return rc;
   if (!ra.fuse_select) {
@@ -314,7 +316,8 @@ int forward_impl(k3moe_layer* L, const void* x, int T, float* y, cudaStream_t s)
     rc = make_resident(L, s);
     if (rc) return rc;
   }
-  FfnArgs fa{L->eptr_dev, D.d, D.f, D.E, D.k, T, L->ws, y, L->num_sms, L->wait_ns, L->test_stall, L->ring_depth};
+  FfnArgs fa{L->eptr_dev, D.d, D.f, D.E, D.k, T, L->ws, y, L->num_sms, L->wait_ns, L->test_stall, L->ring_depth,
+             L->zero_scales ? 1 : 0};
   L->test_stall = 0;
   rc = timed_launch(L, KID_GATEUP, s, [&] { return launch_gateup(fa, s); });
   if (rc) return rc;
@@ -509,7 +512,8 @@ int k3moe_pack_experts(const k3moe_dims* dims, const void* canon_nib, const void
   cudaFree(stage_scl);
   cudaFree(stage_out);
   if (!ok) return bail(fail(K3MOE_ERR_CUDA, "packing failed: %s", cudaGetErrorString(cudaGetLastError())));
-  if (bad) return bail(fail(K3MOE_ERR_INVALID_ARG, "a scale byte is 255 (E8M0 NaN)"));
+  if (bad & 1) return bail(fail(K3MOE_ERR_INVALID_ARG, "a scale byte is 255 (E8M0 NaN)"));
+  L->zero_scales = (bad & 2) != 0;
   if (!cache) {
     std::vector<const uint8_t*> ptrs(D.E);
     for (int e = 0; e < D.E; ++e) ptrs[e] = L->packed + (size_t)e * eb;

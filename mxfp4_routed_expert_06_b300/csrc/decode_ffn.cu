@@ -11,7 +11,7 @@
 // into a zeroed fp32 fragment that is added, times the scale, to the running sum.  fp16 x
 // fp16 products are exact and every sum is fp32.
 //
-// Both FFN kernels are persistent (one CTA per SM); a CTA walks tasks
+// Both FFN kernels are persistent (two CTAs per SM); a CTA walks tasks
 // i = blockIdx.x + j*gridDim.x.  Each consumer warp streams its own stages from HBM with
 // cp.async (16 bytes per lane, L2 evict-first) several stages ahead into a private shared-memory
 // ring; on this GPU that keeps ~7 TB/s in flight, where a single-thread bulk-copy producer is
@@ -122,6 +122,14 @@ __device__ __forceinline__ void mma_zero(float (&d)[4], const uint32_t (&a)[4], 
 // E8M0 byte -> 2^(s-127) as fp32 (s = 0 is the subnormal 2^-127).
 __device__ __forceinline__ float e8m0f(uint32_t s) { return __uint_as_float(s ? (s << 23) : 0x00400000u); }
 
+// Scale byte b (0..3) of a word of four E8M0 bytes, as fp32.  ZS = false when the layer has no
+// zero scale byte (checked at pack time): then 2^(s-127) is just s placed in the exponent field.
+template <bool ZS>
+__device__ __forceinline__ float scale_of(uint32_t w4, int b) {
+  const uint32_t s = __byte_perm(w4, 0u, 0x4440u + (uint32_t)b);
+  return ZS ? e8m0f(s) : __uint_as_float(s << 23);
+}
+
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int s) {
   return s == 0 ? v.x : (s == 1 ? v.y : (s == 2 ? v.z : v.w));
 }
@@ -163,17 +171,6 @@ template <int N>
 __device__ __forceinline__ void cp_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
-__device__ __forceinline__ void cp_wait_dyn(int n) {
-  // wait until at most n (< kMaxDepth) of this thread's copy groups are pending
-  switch (n) {
-    case 0: cp_wait<0>(); break;
-    case 1: cp_wait<1>(); break;
-    case 2: cp_wait<2>(); break;
-    case 3: cp_wait<3>(); break;
-    case 4: cp_wait<4>(); break;
-    default: cp_wait<5>(); break;
-  }
-}
 // the warp copies `bytes` (multiple of 16) from src to dst, 16 bytes per lane per step
 __device__ __forceinline__ void warp_copy(uint8_t* dst, const uint8_t* src, int bytes, int lane, uint64_t pol) {
   for (int off = lane * 16; off < bytes; off += 512) cp16(dst + off, src + off, pol);
@@ -208,8 +205,8 @@ __device__ __forceinline__ float d_w(const DescRegs& r, int m) {
 // ------------------------------------------------------------------------ gate/up ---
 // Each consumer warp streams its own stages (cp.async, `depth` stages ahead) into a private
 // ring, so nothing is shared on the data path.  Warp w owns k-tiles kt % 8 == w of every task.
-constexpr int kGuRed = 8;                            // partial-sum slots (multiple of kGuEpi)
-constexpr int kGuEpi = 4;                            // epilogue warps; task j -> warp j % kGuEpi
+constexpr int kGuRed = 4;                            // partial-sum slots (multiple of kGuEpi)
+constexpr int kGuEpi = 2;                            // epilogue warps; task j -> warp j % kGuEpi
 constexpr int kGuThreads = (kConsumers + kGuEpi) * 32;
 constexpr int kGuTileBytes = 2 * kTileBytes;         // gate tile + up tile of one (row group, k-tile)
 
@@ -232,8 +229,9 @@ inline GuLayout gu_layout(int mcap, size_t budget) {
 // k-tiles of warp w among the KT k-tiles of one task (kt % 8 == w)
 __device__ __forceinline__ int warp_kts(int KT, int w) { return w < KT ? (KT - w + kConsumers - 1) / kConsumers : 0; }
 
-__global__ void __launch_bounds__(kGuThreads, 1) gateup_kernel(FfnArgs a, GuLayout L) {
-  extern __shared__ __align__(1024) uint8_t smem[];
+template <int DEPTH, bool ZS>
+__global__ void __launch_bounds__(kGuThreads, 2) gateup_kernel(FfnArgs a, GuLayout L) {
+  extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* red_full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* red_empty = red_full + kGuRed;
   uint64_t* never = red_empty + kGuRed;
@@ -284,9 +282,8 @@ __global__ void __launch_bounds__(kGuThreads, 1) gateup_kernel(FfnArgs a, GuLayo
       if (my_tasks > 1) dnext = load_desc(a.ws.units + (blockIdx.x + G) / RG, lane);
       Wcur = a.expert_ptr[d_e(dcur)] + (size_t)(blockIdx.x % RG) * gu_stride;
     }
-    auto issue_next = [&](long long sidx) {
-      // copy stage sidx (= the issue cursor) into its ring slot, then advance the cursor
-      uint8_t* st = ring + (size_t)(sidx % L.depth) * L.stage_bytes;
+    auto issue_next = [&](uint8_t* st) {
+      // copy the stage at the issue cursor into `st`, then advance the cursor
       const int kt = warp + kConsumers * ci;
       warp_copy(st, Wcur + (size_t)kt * kGuTileBytes, kGuTileBytes, lane, pol_w);
       const int M = d_M(dcur);
@@ -302,25 +299,28 @@ __global__ void __launch_bounds__(kGuThreads, 1) gateup_kernel(FfnArgs a, GuLayo
         if (ji + 1 < my_tasks) dnext = load_desc(a.ws.units + (blockIdx.x + (ji + 1) * G) / RG, lane);
       }
     };
+    // DEPTH groups are always committed ahead (empty ones when there is nothing left to copy),
+    // so the stage being consumed is always DEPTH-1 groups behind the newest.
     long long issued = 0;
-    for (; issued < nstages && issued < L.depth; ++issued) {
-      issue_next(issued);
+#pragma unroll
+    for (int i = 0; i < DEPTH; ++i) {
+      if (issued < nstages) {
+        issue_next(ring + (size_t)i * L.stage_bytes);
+        ++issued;
+      }
       cp_commit();
     }
 
-    // every consume step commits one (possibly empty) group, so the group of the stage being
-    // consumed is always followed by exactly min(depth, nstages) - 1 newer groups
-    const int wait_n = (int)(nstages < L.depth ? nstages : L.depth) - 1;
-    long long consumed = 0;
+    int rslot = 0;
     int M_n = my_tasks > 0 ? __ldg(&a.ws.units[blockIdx.x / RG].M) : 0;
     for (int j = 0; j < my_tasks; ++j) {
       const int M = M_n;
       if (j + 1 < my_tasks) M_n = __ldg(&a.ws.units[(blockIdx.x + (j + 1) * G) / RG].M);
       float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      for (int c = 0; c < cw; ++c, ++consumed) {
-        cp_wait_dyn(wait_n);
+      for (int c = 0; c < cw; ++c) {
+        cp_wait<DEPTH - 1>();
         __syncwarp();
-        const uint8_t* st = ring + (size_t)(consumed % L.depth) * L.stage_bytes;
+        uint8_t* st = ring + (size_t)rslot * L.stage_bytes;
         uint4 nib[2][2];
         uint2 sc[2];
 #pragma unroll
@@ -335,10 +335,11 @@ __global__ void __launch_bounds__(kGuThreads, 1) gateup_kernel(FfnArgs a, GuLayo
           xv[b] = g < M ? lds128(st + kGuTileBytes + g * 256 + (b * 4 + t) * 16) : make_uint4(0, 0, 0, 0);
         __syncwarp();
         if (issued < nstages) {  // refill the slot just read
-          issue_next(issued);
+          issue_next(st);
           ++issued;
         }
         cp_commit();
+        rslot = rslot + 1 == DEPTH ? 0 : rslot + 1;
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
           float bacc[2][4];
@@ -358,8 +359,8 @@ __global__ void __launch_bounds__(kGuThreads, 1) gateup_kernel(FfnArgs a, GuLayo
           }
 #pragma unroll
           for (int m = 0; m < 2; ++m) {
-            const float s_lo = e8m0f((sc[m].x >> (8 * b)) & 0xFFu);
-            const float s_hi = e8m0f((sc[m].y >> (8 * b)) & 0xFFu);
+            const float s_lo = scale_of<ZS>(sc[m].x, b);
+            const float s_hi = scale_of<ZS>(sc[m].y, b);
             acc[m][0] = fmaf(bacc[m][0], s_lo, acc[m][0]);
             acc[m][1] = fmaf(bacc[m][1], s_lo, acc[m][1]);
             acc[m][2] = fmaf(bacc[m][2], s_hi, acc[m][2]);
@@ -510,8 +511,9 @@ inline DnLayout dn_layout(int f, int mcap, size_t budget) {
   return L;
 }
 
-__global__ void __launch_bounds__(kDnThreads, 1) down_kernel(FfnArgs a, DnLayout L) {
-  extern __shared__ __align__(1024) uint8_t smem[];
+template <int DEPTH, bool ZS>
+__global__ void __launch_bounds__(kDnThreads, 2) down_kernel(FfnArgs a, DnLayout L) {
+  extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   uint32_t* err = a.ws.sync + 1;
@@ -555,8 +557,7 @@ __global__ void __launch_bounds__(kDnThreads, 1) down_kernel(FfnArgs a, DnLayout
     if (my_tasks > 1) dnext = load_desc(a.ws.units + (first + step) / RG, lane);
     Wcur = a.expert_ptr[d_e(dcur)] + gu_bytes + (size_t)(first % RG) * KT * kTileBytes;
   }
-  auto issue_next = [&](long long sidx) {
-    uint8_t* st = ring + (size_t)(sidx % L.depth) * L.stage_bytes;
+  auto issue_next = [&](uint8_t* st) {
     const int kt0 = ci * L.kc, nk = min(L.kc, KT - kt0);
     warp_copy(st, Wcur + (size_t)kt0 * kTileBytes, nk * kTileBytes, lane, pol_w);
     const int M = d_M(dcur);
@@ -576,14 +577,18 @@ __global__ void __launch_bounds__(kDnThreads, 1) down_kernel(FfnArgs a, DnLayout
       if (ji + 1 < my_tasks) dnext = load_desc(a.ws.units + (first + (ji + 1) * step) / RG, lane);
     }
   };
+  // DEPTH groups always committed ahead (see gateup_kernel)
   long long issued = 0;
-  for (; issued < nstages && issued < L.depth; ++issued) {
-    issue_next(issued);
+#pragma unroll
+  for (int i = 0; i < DEPTH; ++i) {
+    if (issued < nstages) {
+      issue_next(ring + (size_t)i * L.stage_bytes);
+      ++issued;
+    }
     cp_commit();
   }
 
-  const int wait_n = (int)(nstages < L.depth ? nstages : L.depth) - 1;
-  long long consumed = 0;
+  int rslot = 0;
   DescRegs dtask = my_tasks > 0 ? load_desc(a.ws.units + first / RG, lane) : DescRegs{0, 0};
   for (int j = 0; j < my_tasks; ++j) {
     const int i = first + j * step;
@@ -593,10 +598,10 @@ __global__ void __launch_bounds__(kDnThreads, 1) down_kernel(FfnArgs a, DnLayout
     const int rg = i % RG;
     const int n0 = 2 * t, n1 = 2 * t + 1;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int c = 0; c < L.nch; ++c, ++consumed) {
-      cp_wait_dyn(wait_n);
+    for (int c = 0; c < L.nch; ++c) {
+      cp_wait<DEPTH - 1>();
       __syncwarp();
-      const uint8_t* st = ring + (size_t)(consumed % L.depth) * L.stage_bytes;
+      uint8_t* st = ring + (size_t)rslot * L.stage_bytes;
       const uint8_t* hrow = st + wb + g * L.kc * 256;
       const float* hs = reinterpret_cast<const float*>(st + wb + M * L.kc * 256);
       const float* hs0 = hs + (n0 < M ? n0 : 0) * L.kc * 4;
@@ -616,8 +621,8 @@ __global__ void __launch_bounds__(kDnThreads, 1) down_kernel(FfnArgs a, DnLayout
           mma_zero(bacc, A, hv.x, hv.y);
           dec4(word_of(nv, 2 * (b & 1) + 1), A);
           mma_acc(bacc, A, hv.z, hv.w);
-          const float s_lo = e8m0f((sc.x >> (8 * b)) & 0xFFu);
-          const float s_hi = e8m0f((sc.y >> (8 * b)) & 0xFFu);
+          const float s_lo = scale_of<ZS>(sc.x, b);
+          const float s_hi = scale_of<ZS>(sc.y, b);
           const float h0 = n0 < M ? hs0[4 * kk + b] : 0.f;
           const float h1 = n1 < M ? hs1[4 * kk + b] : 0.f;
           acc[0] = fmaf(bacc[0], s_lo * h0, acc[0]);
@@ -628,10 +633,11 @@ __global__ void __launch_bounds__(kDnThreads, 1) down_kernel(FfnArgs a, DnLayout
       }
       __syncwarp();
       if (issued < nstages) {
-        issue_next(issued);
+        issue_next(st);
         ++issued;
       }
       cp_commit();
+      rslot = rslot + 1 == DEPTH ? 0 : rslot + 1;
     }
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
@@ -648,7 +654,7 @@ __global__ void __launch_bounds__(kDnThreads, 1) down_kernel(FfnArgs a, DnLayout
 }
 
 // ------------------------------------------------------------------------- combine ---
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ obuf, int T, int d, int k,
+__global__ void __launch_bounds__(64) combine_kernel(const float* __restrict__ obuf, int T, int d, int k,
                                                       float* __restrict__ y) {
   const size_t n4 = (size_t)T * d / 4;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
@@ -666,48 +672,86 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   }
 }
 
-constexpr size_t kSmemBudget = 220 * 1024;
+// two CTAs per SM: 2 x (110 KB + static + 1 KB reserved) fits the SM's 228 KB of shared memory
+constexpr int kCtasPerSm = 2;
+constexpr size_t kSmemBudget = 110 * 1024;
+
+}  // namespace
+
+namespace {
+
+// Ring depths with an instantiated kernel; the layout's depth is rounded down to one of them.
+constexpr int kDepths[] = {2, 3, 4, 6};
+
+template <typename Layout>
+int pick_depth(Layout& L, int requested) {
+  int d = requested > 0 && requested < L.depth ? requested : L.depth;
+  int best = 2;
+  for (int v : kDepths)
+    if (v <= d) best = v;
+  return best;
+}
+
+template <int DEPTH, bool ZS>
+cudaError_t launch_gu(const FfnArgs& a, const GuLayout& L, cudaStream_t s) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e =
+        cudaFuncSetAttribute(gateup_kernel<DEPTH, ZS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  gateup_kernel<DEPTH, ZS><<<a.num_sms * kCtasPerSm, kGuThreads, L.total, s>>>(a, L);
+  return cudaGetLastError();
+}
+
+template <int DEPTH, bool ZS>
+cudaError_t launch_dn(const FfnArgs& a, const DnLayout& L, cudaStream_t s) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e =
+        cudaFuncSetAttribute(down_kernel<DEPTH, ZS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  down_kernel<DEPTH, ZS><<<a.num_sms * kCtasPerSm, kDnThreads, L.total, s>>>(a, L);
+  return cudaGetLastError();
+}
 
 }  // namespace
 
 cudaError_t launch_gateup(const FfnArgs& a, cudaStream_t s) {
   const int mcap = a.T < kUnitTokens ? a.T : kUnitTokens;
   GuLayout L = gu_layout(mcap, kSmemBudget);
-  if (a.ring_depth > 0 && a.ring_depth < L.depth) {
-    L.depth = a.ring_depth;
-    L.total = L.ring_off + (size_t)kConsumers * L.depth * L.stage_bytes;
+  L.depth = pick_depth(L, a.ring_depth);
+  L.total = L.ring_off + (size_t)kConsumers * L.depth * L.stage_bytes;
+  const bool zs = a.zero_scales != 0;
+  switch (L.depth) {
+    case 2: return zs ? launch_gu<2, true>(a, L, s) : launch_gu<2, false>(a, L, s);
+    case 3: return zs ? launch_gu<3, true>(a, L, s) : launch_gu<3, false>(a, L, s);
+    case 4: return zs ? launch_gu<4, true>(a, L, s) : launch_gu<4, false>(a, L, s);
+    default: return zs ? launch_gu<6, true>(a, L, s) : launch_gu<6, false>(a, L, s);
   }
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  gateup_kernel<<<a.num_sms, kGuThreads, L.total, s>>>(a, L);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_down(const FfnArgs& a, cudaStream_t s) {
   const int mcap = a.T < kUnitTokens ? a.T : kUnitTokens;
   DnLayout L = dn_layout(a.f, mcap, kSmemBudget);
-  if (a.ring_depth > 0 && a.ring_depth < L.depth) {
-    L.depth = a.ring_depth;
-    L.total = (size_t)kConsumers * L.depth * L.stage_bytes;
+  L.depth = pick_depth(L, a.ring_depth);
+  L.total = (size_t)kConsumers * L.depth * L.stage_bytes;
+  const bool zs = a.zero_scales != 0;
+  switch (L.depth) {
+    case 2: return zs ? launch_dn<2, true>(a, L, s) : launch_dn<2, false>(a, L, s);
+    case 3: return zs ? launch_dn<3, true>(a, L, s) : launch_dn<3, false>(a, L, s);
+    case 4: return zs ? launch_dn<4, true>(a, L, s) : launch_dn<4, false>(a, L, s);
+    default: return zs ? launch_dn<6, true>(a, L, s) : launch_dn<6, false>(a, L, s);
   }
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  down_kernel<<<a.num_sms, kDnThreads, L.total, s>>>(a, L);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_combine(const FfnArgs& a, cudaStream_t s) {
   const size_t n4 = (size_t)a.T * a.d / 4;
-  const int grid = (int)std::min<size_t>((n4 + 255) / 256, (size_t)a.num_sms * 8);
-  combine_kernel<<<grid, 256, 0, s>>>(a.ws.obuf, a.T, a.d, a.k, a.y);
+  const int grid = (int)std::min<size_t>((n4 + 63) / 64, (size_t)a.num_sms * 32);
+  combine_kernel<<<grid, 64, 0, s>>>(a.ws.obuf, a.T, a.d, a.k, a.y);
   return cudaGetLastError();
 }
 

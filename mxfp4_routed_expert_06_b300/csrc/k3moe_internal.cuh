@@ -127,6 +127,7 @@ struct FfnArgs {
   unsigned long long wait_ns;        // bound on every device-side wait
   int test_stall;                    // 1: consumers wait on a barrier nothing arrives at (timeout test)
   int ring_depth;                    // 0: automatic; else stages in flight per streaming warp
+  int zero_scales;                   // 1: some E8M0 scale byte is 0 (exact subnormal decode needed)
 };
 cudaError_t launch_gateup(const FfnArgs& a, cudaStream_t s);
 cudaError_t launch_down(const FfnArgs& a, cudaStream_t s);

@@ -80,9 +80,19 @@ __global__ void __launch_bounds__(kWarps * 32) router_topk_noalloc_kernel(
   float* ks = keys + (size_t)warp * E;
   for (int t = warp; t < T; t += kWarps) {
     const float* row = logits + (size_t)t * E;
-    for (int j = lane; j < E; j += 32) {
-      const float s = sig(__ldcg(row + j));
-      ks[j] = bias ? s + __ldg(bias + j) : s;
+    for (int j0 = 0; j0 < E; j0 += 32 * 16) {  // 16 loads in flight per lane
+      float z[16], bb[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const int j = j0 + 32 * q + lane;
+        z[q] = j < E ? __ldcg(row + j) : 0.f;
+        bb[q] = (bias && j < E) ? __ldg(bias + j) : 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const int j = j0 + 32 * q + lane;
+        if (j < E) ks[j] = sig(z[q]) + bb[q];
+      }
     }
     __syncwarp();
     int mine = -1;

@@ -64,7 +64,8 @@ __global__ void pack_kernel(const uint8_t* __restrict__ canon_nib, const uint8_t
       const int row = rowb + g + 8 * h;
       for (int b = 0; b < 4; ++b) {
         const uint32_t sv = scl[(size_t)row * sb + kt * 4 + b];
-        if (sv == 255u) atomicExch(bad, 1);
+        if (sv == 255u) atomicOr(bad, 1);  // E8M0 NaN: refused
+        if (sv == 0u) atomicOr(bad, 2);    // 2^-127: kernels take the exact subnormal path
         word |= sv << (8 * b);
       }
     }

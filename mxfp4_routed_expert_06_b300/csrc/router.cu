@@ -5,21 +5,25 @@
 // experts are mixed with weights from the unbiased scores, renormalised to sum 1.  The pages
 // pick 16 of 896 experts (glossary entry MoE).
 //
-// GPU design: the router is a GEMV over W_r (fp32, [E][d]) with one warp per expert row and
-// the tokens in tiles of 4, so W_r is read once per call (it stays in L2 across calls).  For
+// GPU design: the router is a GEMV over W_r (fp32, [E][d]) with two warps per expert row (one
+// per half of d, 14 loads in flight per lane) and the tokens staged in shared memory 4 at a time,
+// so W_r is read once per call.  The same pass converts each token to fp16 fragments.  For
 // small T the last CTA to finish (atomic ticket) also runs the top-k and the bucketing, which
 // saves two launches on the single-token path.  Top-k is a warp per token: k rounds of a
 // warp-wide (key desc, id asc) argmax over the keys kept in shared memory.  Bucketing is
 // deterministic: counts by shared-memory atomics (order-free), an exclusive scan, and a
 // stable scatter in rounds where __match_any_sync ranks equal experts inside a warp and the
 // warps of a round take their turn in order.
+#include <algorithm>
+
 #include "k3moe_internal.cuh"
 
 namespace k3 {
 namespace {
 
-constexpr int kRouterWarps = 4;  // expert rows per CTA, one per warp
-constexpr int kTokTile = 4;
+constexpr int kRouterWarps = 8;  // 2 warps per expert row (each half of d)
+constexpr int kRowsPerCta = kRouterWarps / 2;
+constexpr int kTokTile = 4;      // tokens staged in shared memory at a time
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
@@ -36,27 +40,91 @@ __device__ __forceinline__ int fp16_scale_exp(float m) {
 }
 __device__ __forceinline__ float exp2i(int q) { return __uint_as_float((uint32_t)(127 + q) << 23); }
 
-// --------------------------------------------------------------------------- logits ---
-__device__ void logits_rows(const RouterArgs& a) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = blockIdx.x * kRouterWarps + warp;
-  if (e >= a.E) return;
-  const float4* wr = reinterpret_cast<const float4*>(a.Wr + (size_t)e * a.d);
-  const int nq = a.d / 4;
-  for (int t0 = 0; t0 < a.T; t0 += kTokTile) {
-    float acc[kTokTile] = {0.f, 0.f, 0.f, 0.f};
-    const int nt = min(kTokTile, a.T - t0);
-#pragma unroll 8
-    for (int q = lane; q < nq; q += 32) {
-      const float4 w = __ldg(wr + q);
+// Stage tokens [t0, t0+nt) of x (bf16) into shared memory with 16-byte loads.
+__device__ void stage_tokens(const RouterArgs& a, int t0, int nt, uint16_t* xs) {
+  const int n16 = nt * a.d / 8;
+  const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)t0 * a.d);
+  uint4* dst = reinterpret_cast<uint4*>(xs);
+  for (int i = threadIdx.x; i < n16; i += blockDim.x) dst[i] = __ldg(src + i);
+}
+
+// x row (bf16, in shared memory) -> fp16 B-fragment row with a per-token power-of-two scale.
+__device__ void convert_token(const RouterArgs& a, int t, const uint16_t* xr, float* red) {
+  float m = 0.f;
+  for (int j = threadIdx.x * 2; j < a.d; j += blockDim.x * 2) {
+    const uint32_t v = *reinterpret_cast<const uint32_t*>(xr + j);
+    m = fmaxf(m, fmaxf(fabsf(bf16_lo(v)), fabsf(bf16_hi(v))));
+  }
 #pragma unroll
-      for (int tt = 0; tt < kTokTile; ++tt) {
-        if (tt < nt) {
-          const uint2 xv = __ldg(reinterpret_cast<const uint2*>(a.x + (size_t)(t0 + tt) * a.d) + q);
-          acc[tt] = fmaf(bf16_lo(xv.x), w.x, acc[tt]);
-          acc[tt] = fmaf(bf16_hi(xv.x), w.y, acc[tt]);
-          acc[tt] = fmaf(bf16_lo(xv.y), w.z, acc[tt]);
-          acc[tt] = fmaf(bf16_hi(xv.y), w.w, acc[tt]);
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  m = red[0];
+  for (int i = 1; i < (int)(blockDim.x >> 5); ++i) m = fmaxf(m, red[i]);
+  const int q = fp16_scale_exp(m);
+  const float inv = exp2i(-q);
+  const int items = (a.d / 32) * 4;
+  for (int it = threadIdx.x; it < items; it += blockDim.x) {
+    const int blk = it >> 2, tq = it & 3;
+    __align__(16) __half h[8];
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      const int kb = 32 * blk + 16 * s + 2 * tq;
+      const uint32_t p0 = *reinterpret_cast<const uint32_t*>(xr + kb);
+      const uint32_t p1 = *reinterpret_cast<const uint32_t*>(xr + kb + 8);
+      h[4 * s + 0] = __float2half_rn(bf16_lo(p0) * inv);
+      h[4 * s + 1] = __float2half_rn(bf16_hi(p0) * inv);
+      h[4 * s + 2] = __float2half_rn(bf16_lo(p1) * inv);
+      h[4 * s + 3] = __float2half_rn(bf16_hi(p1) * inv);
+    }
+    *reinterpret_cast<uint4*>(a.ws.xfrag + (size_t)t * a.d + (size_t)it * 8) = *reinterpret_cast<uint4*>(h);
+  }
+  if (threadIdx.x == 0) a.ws.xscale[t] = exp2i(q);
+  __syncthreads();
+}
+
+// --------------------------------------------------------------------------- logits ---
+// CTA = kRowsPerCta expert rows; warp w handles row w/2, half w%2 of d; the two halves are added
+// in a fixed order.  Tokens are staged kTokTile at a time; the CTA with blockIdx == t % grid
+// also converts token t to fp16 fragments.
+__device__ void logits_and_convert(const RouterArgs& a, uint16_t* xs, float* red, float* half_sum) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * kRowsPerCta + (warp >> 1);
+  const int hf = warp & 1;
+  const int nq = a.d / 4, q0 = hf * (nq / 2), q1 = q0 + nq / 2;
+  const float4* wr = reinterpret_cast<const float4*>(a.Wr + (size_t)(e < a.E ? e : 0) * a.d);
+  for (int t0 = 0; t0 < a.T; t0 += kTokTile) {
+    const int nt = min(kTokTile, a.T - t0);
+    __syncthreads();
+    stage_tokens(a, t0, nt, xs);
+    __syncthreads();
+    for (int tt = 0; tt < nt; ++tt)
+      if ((t0 + tt) % (int)gridDim.x == (int)blockIdx.x) convert_token(a, t0 + tt, xs + (size_t)tt * a.d, red);
+    float acc[kTokTile] = {0.f, 0.f, 0.f, 0.f};
+    if (e < a.E) {
+      constexpr int kB = 14;  // W_r loads in flight per lane
+      for (int qb = q0 + lane; qb < q1; qb += 32 * kB) {
+        float4 wv[kB];
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+          const int q = qb + 32 * j;
+          wv[j] = q < q1 ? __ldg(wr + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+          const int q = qb + 32 * j;
+          if (q < q1) {
+#pragma unroll
+            for (int tt = 0; tt < kTokTile; ++tt) {
+              if (tt < nt) {
+                const uint2 xv = *reinterpret_cast<const uint2*>(xs + (size_t)tt * a.d + 4 * q);
+                acc[tt] = fmaf(bf16_lo(xv.x), wv[j].x, acc[tt]);
+                acc[tt] = fmaf(bf16_hi(xv.x), wv[j].y, acc[tt]);
+                acc[tt] = fmaf(bf16_lo(xv.y), wv[j].z, acc[tt]);
+                acc[tt] = fmaf(bf16_hi(xv.y), wv[j].w, acc[tt]);
+              }
+            }
+          }
         }
       }
     }
@@ -65,147 +133,283 @@ __device__ void logits_rows(const RouterArgs& a) {
       float v = acc[tt];
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-      if (lane == 0 && tt < nt) a.ws.logits[(size_t)(t0 + tt) * a.E + e] = v;
+      if (lane == 0) half_sum[warp * kTokTile + tt] = v;
     }
-  }
-}
-
-// x (bf16) -> fp16 B-fragment rows with a per-token power-of-two scale.
-__device__ void convert_tokens(const RouterArgs& a, float* red) {
-  for (int t = blockIdx.x; t < a.T; t += gridDim.x) {
-    const uint16_t* xr = a.x + (size_t)t * a.d;
-    float m = 0.f;
-    for (int j = threadIdx.x; j < a.d; j += blockDim.x) m = fmaxf(m, fabsf(__uint_as_float((uint32_t)xr[j] << 16)));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
     __syncthreads();
-    m = red[0];
-    for (int i = 1; i < (int)(blockDim.x >> 5); ++i) m = fmaxf(m, red[i]);
-    __syncthreads();
-    const int q = fp16_scale_exp(m);
-    const float inv = exp2i(-q);
-    const int items = (a.d / 32) * 4;
-    for (int it = threadIdx.x; it < items; it += blockDim.x) {
-      const int blk = it >> 2, tq = it & 3;
-      __align__(16) __half h[8];
-#pragma unroll
-      for (int s = 0; s < 2; ++s) {
-        const int kb = 32 * blk + 16 * s + 2 * tq;
-        h[4 * s + 0] = __float2half_rn(__uint_as_float((uint32_t)xr[kb] << 16) * inv);
-        h[4 * s + 1] = __float2half_rn(__uint_as_float((uint32_t)xr[kb + 1] << 16) * inv);
-        h[4 * s + 2] = __float2half_rn(__uint_as_float((uint32_t)xr[kb + 8] << 16) * inv);
-        h[4 * s + 3] = __float2half_rn(__uint_as_float((uint32_t)xr[kb + 9] << 16) * inv);
-      }
-      *reinterpret_cast<uint4*>(a.ws.xfrag + (size_t)t * a.d + (size_t)it * 8) = *reinterpret_cast<uint4*>(h);
-    }
-    if (threadIdx.x == 0) a.ws.xscale[t] = exp2i(q);
+    if (hf == 0 && lane < nt && e < a.E)
+      a.ws.logits[(size_t)(t0 + lane) * a.E + e] = half_sum[warp * kTokTile + lane] + half_sum[(warp + 1) * kTokTile + lane];
   }
 }
 
 }  // namespace
 
 // ---------------------------------------------------------------------------- top-k ---
-// One warp selects the k largest keys of one token.  ks: E floats of this warp's shared memory.
-__device__ void topk_warp(const float* logits_row, const float* bias, int E, int k, float* ks, int32_t* idx_out,
-                          float* w_out) {
+// Key as an unsigned integer with the same order as the float (larger key -> larger integer).
+__device__ __forceinline__ uint32_t ord_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// a is ranked before b: larger key, or equal key and lower expert id
+__device__ __forceinline__ bool ranks_before(uint32_t ua, int ia, uint32_t ub, int ib) {
+  return ua > ub || (ua == ub && ia < ib);
+}
+
+// Bitonic sort of the warp's 32*R (key, id) pairs into rank order (best first); element
+// i = 32*j + lane lives in register j of lane `lane`.
+template <int R>
+__device__ __forceinline__ void warp_sort(uint32_t (&u)[R], int (&id)[R]) {
   const int lane = threadIdx.x & 31;
-  for (int e = lane; e < E; e += 32) {
-    const float s = sigmoidf_acc(__ldcg(logits_row + e));
-    ks[e] = bias ? s + __ldg(bias + e) : s;
+#pragma unroll
+  for (int size = 2; size <= 32 * R; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      if (stride >= 32) {
+        const int js = stride / 32;
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+          const int jp = j ^ js;
+          if (j < jp) {
+            const bool asc = (((32 * j + lane) & size) == 0);  // block ordered best-first
+            const bool swap = asc ? ranks_before(u[jp], id[jp], u[j], id[j]) : ranks_before(u[j], id[j], u[jp], id[jp]);
+            if (swap) {
+              const uint32_t tu = u[j];
+              const int ti = id[j];
+              u[j] = u[jp];
+              id[j] = id[jp];
+              u[jp] = tu;
+              id[jp] = ti;
+            }
+          }
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+          const uint32_t ou = __shfl_xor_sync(0xffffffffu, u[j], stride);
+          const int oi = __shfl_xor_sync(0xffffffffu, id[j], stride);
+          const int i = 32 * j + lane;
+          const bool keep_first = (((i & size) == 0) == ((i & stride) == 0));
+          if (keep_first != ranks_before(u[j], id[j], ou, oi)) {
+            u[j] = ou;
+            id[j] = oi;
+          }
+        }
+      }
+    }
   }
-  __syncwarp();
-  int mine = -1;
-  for (int i = 0; i < k; ++i) {
-    float bk = -INFINITY;
-    int bi = 0x7fffffff;
-    for (int e = lane; e < E; e += 32) {
-      const float v = ks[e];
-      if (v > bk || (v == bk && e < bi)) { bk = v; bi = e; }
+}
+
+// Merge a ranked 32-list held one per lane (a) with another (b) into the ranked best 32 of both.
+__device__ __forceinline__ void warp_merge32(uint32_t& au, int& ai, uint32_t bu, int bi) {
+  const int lane = threadIdx.x & 31;
+  // a ascending by rank, b reversed: the elementwise better of the two is a bitonic sequence
+  // holding the best 32 of the union
+  const uint32_t ru = __shfl_sync(0xffffffffu, bu, 31 - lane);
+  const int ri = __shfl_sync(0xffffffffu, bi, 31 - lane);
+  if (ranks_before(ru, ri, au, ai)) {
+    au = ru;
+    ai = ri;
+  }
+#pragma unroll
+  for (int stride = 16; stride > 0; stride >>= 1) {
+    const uint32_t ou = __shfl_xor_sync(0xffffffffu, au, stride);
+    const int oi = __shfl_xor_sync(0xffffffffu, ai, stride);
+    const bool keep_first = (lane & stride) == 0;
+    if (keep_first != ranks_before(au, ai, ou, oi)) {
+      au = ou;
+      ai = oi;
+    }
+  }
+}
+
+constexpr int kTopkThreads = 256;
+constexpr int kSortR = 4;  // per-warp sort chunk: 32 * kSortR keys
+
+// The whole block selects the k largest keys (k <= 32) of one token.  Shared memory: ku/sg =
+// E words each (ordered keys, unbiased sigmoid scores), cand = 8 * 32 (key, id) pairs.  Each
+// thread scores E/256 experts; each warp sorts its slice in chunks of 128 and keeps a ranked
+// top-32; the 8 lists are merged by warp 0.  The picks go to idx_out/w_out (global) and, when
+// given, to the shared-memory copies idx_s/w_s.
+__device__ void topk_block(const float* logits_row, const float* bias, int E, int k, uint32_t* ku, float* sg,
+                           uint2* cand, int32_t* idx_out, float* w_out, int32_t* idx_s = nullptr,
+                           float* w_s = nullptr) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nw = blockDim.x >> 5;
+  // scores: every thread issues all of its loads before using any of them
+  constexpr int kB = 8;
+  for (int e0 = 0; e0 < E; e0 += (int)blockDim.x * kB) {
+    float z[kB], b[kB];
+#pragma unroll
+    for (int j = 0; j < kB; ++j) {
+      const int e = e0 + (int)blockDim.x * j + tid;
+      z[j] = e < E ? __ldcg(logits_row + e) : 0.f;
+      b[j] = (bias && e < E) ? __ldg(bias + e) : 0.f;
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ok = __shfl_xor_sync(0xffffffffu, bk, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      if (ok > bk || (ok == bk && oi < bi)) { bk = ok; bi = oi; }
+    for (int j = 0; j < kB; ++j) {
+      const int e = e0 + (int)blockDim.x * j + tid;
+      if (e < E) {
+        const float s = sigmoidf_acc(z[j]);
+        sg[e] = s;
+        ku[e] = ord_key(s + b[j]);
+      }
     }
-    if (lane == i) mine = bi;
-    __syncwarp();
-    if (lane == 0 && bi < E) ks[bi] = -INFINITY;
-    __syncwarp();
   }
-  const float sg = (lane < k && mine >= 0) ? sigmoidf_acc(__ldcg(logits_row + mine)) : 0.f;
-  float tot = sg;
+  __syncthreads();
+  // per-warp ranked top-32 of its slice
+  const int per = (E + nw - 1) / nw;
+  const int ea = min(E, warp * per), eb = min(E, ea + per);
+  uint32_t bu = 0u;
+  int bi = 0x7fffffff;
+  for (int c0 = ea; c0 < eb; c0 += 32 * kSortR) {
+    uint32_t u[kSortR];
+    int id[kSortR];
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
-  if (lane < k) {
-    idx_out[lane] = mine;
-    w_out[lane] = sg / tot;
+    for (int j = 0; j < kSortR; ++j) {
+      const int e = c0 + 32 * j + lane;
+      const bool in = e < eb;
+      u[j] = in ? ku[e] : 0u;
+      id[j] = in ? e : 0x7fffffff;
+    }
+    warp_sort<kSortR>(u, id);
+    warp_merge32(bu, bi, u[0], id[0]);
   }
-  __syncwarp();
+  cand[warp * 32 + lane] = make_uint2(bu, (uint32_t)bi);
+  __syncthreads();
+  if (warp == 0) {
+    uint2 c = cand[lane];
+    uint32_t au = c.x;
+    int ai = (int)c.y;
+    for (int w = 1; w < nw; ++w) {
+      c = cand[w * 32 + lane];
+      warp_merge32(au, ai, c.x, (int)c.y);
+    }
+    const float s = lane < k ? sg[ai] : 0.f;
+    float tot = s;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+    if (lane < k) {
+      const float wv = s / tot;
+      idx_out[lane] = ai;
+      w_out[lane] = wv;
+      if (idx_s) {
+        idx_s[lane] = ai;
+        w_s[lane] = wv;
+      }
+    }
+  }
+  __syncthreads();
 }
 
 // ------------------------------------------------------------------------ bucketing ---
-// Whole-block deterministic bucketing of P picks.  smem: 2*E ints.
+// Whole-block deterministic bucketing of P picks.  smem: 2*E ints, plus P ints when
+// perm_smem (small P: the unit descriptors then read perm from shared memory).
 __device__ void bucket_block(const int32_t* idx, int P, int k, int E, int32_t* counts, int32_t* offsets,
                              int32_t* perm, int32_t* act, int32_t* nact, UnitDesc* units, int32_t* nunits,
-                             const float* w, const float* xscale, int* smem) {
+                             const float* w, const float* xscale, int* smem, bool perm_smem, bool iw_smem = false) {
+  // iw_smem: idx and w are shared-memory arrays of this block (else global, written earlier)
+  auto ld_idx = [&](int p) { return iw_smem ? idx[p] : __ldcg(idx + p); };
+  auto ld_w = [&](int p) { return iw_smem ? w[p] : __ldcg(w + p); };
   __shared__ int s_nunits;
   int* cnt = smem;
   int* cur = smem + E;
+  int* sperm = smem + 2 * E;
   const int tid = threadIdx.x, bd = blockDim.x, warp = tid >> 5, lane = tid & 31, nwarps = bd >> 5;
   for (int e = tid; e < E; e += bd) cnt[e] = 0;
   __syncthreads();
-  for (int p = tid; p < P; p += bd) {
-    const int e = __ldcg(idx + p);
-    if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+  for (int p0 = 0; p0 < P; p0 += bd * 8) {  // 8 loads in flight per thread
+    int ev[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int p = p0 + j * bd + tid;
+      ev[j] = p < P ? ld_idx(p) : -1;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (ev[j] >= 0 && ev[j] < E) atomicAdd(&cnt[ev[j]], 1);
+  }
+  __syncthreads();
+  // block-wide exclusive scan over experts of (picks, active flag, work units); each thread owns
+  // a contiguous range of experts, so every output stays in expert-id order
+  __shared__ int wsum[3][32];
+  const int per = (E + bd - 1) / bd;
+  const int ea = min(E, tid * per), eb = min(E, ea + per);
+  int cs = 0, as = 0, us = 0;
+  for (int e = ea; e < eb; ++e) {
+    const int v = cnt[e];
+    cs += v;
+    as += v > 0;
+    us += (v + kUnitTokens - 1) / kUnitTokens;
+  }
+  int ci = cs, ai = as, ui = us;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int c2 = __shfl_up_sync(0xffffffffu, ci, off), a2 = __shfl_up_sync(0xffffffffu, ai, off),
+              u2 = __shfl_up_sync(0xffffffffu, ui, off);
+    if (lane >= off) {
+      ci += c2;
+      ai += a2;
+      ui += u2;
+    }
+  }
+  if (lane == 31) {
+    wsum[0][warp] = ci;
+    wsum[1][warp] = ai;
+    wsum[2][warp] = ui;
   }
   __syncthreads();
   if (warp == 0) {
-    int run = 0, arun = 0, urun = 0;
-    for (int base = 0; base < E; base += 32) {
-      const int e = base + lane;
-      const int v = e < E ? cnt[e] : 0;
-      const int np = (v + kUnitTokens - 1) / kUnitTokens;  // work units of <= 8 picks
-      int inc = v, uinc = np;
+    int c0 = lane < nwarps ? wsum[0][lane] : 0, a0 = lane < nwarps ? wsum[1][lane] : 0,
+        u0 = lane < nwarps ? wsum[2][lane] : 0;
+    int cc = c0, aa = a0, uu = u0;
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, inc, off);
-        const int uo = __shfl_up_sync(0xffffffffu, uinc, off);
-        if (lane >= off) {
-          inc += o;
-          uinc += uo;
-        }
+    for (int off = 1; off < 32; off <<= 1) {
+      const int c2 = __shfl_up_sync(0xffffffffu, cc, off), a2 = __shfl_up_sync(0xffffffffu, aa, off),
+                u2 = __shfl_up_sync(0xffffffffu, uu, off);
+      if (lane >= off) {
+        cc += c2;
+        aa += a2;
+        uu += u2;
       }
-      const unsigned nz = __ballot_sync(0xffffffffu, v > 0);
-      if (e < E) {
-        cur[e] = run + inc - v;
-        offsets[e] = run + inc - v;
-        counts[e] = v;
-        if (v > 0) act[arun + __popc(nz & ((1u << lane) - 1u))] = e;
-        for (int i = 0; i < np; ++i) {
-          UnitDesc& U = units[urun + uinc - np + i];
-          U.e = e;
-          U.M = min(kUnitTokens, v - i * kUnitTokens);
-          U.pbase = run + inc - v + i * kUnitTokens;
-          U.pad = 0;
-        }
-      }
-      run += __shfl_sync(0xffffffffu, inc, 31);
-      urun += __shfl_sync(0xffffffffu, uinc, 31);
-      arun += __popc(nz);
     }
-    if (lane == 0) {
-      offsets[E] = run;
-      *nact = arun;
-      *nunits = urun;
-      s_nunits = urun;
+    __syncwarp();
+    if (lane < nwarps) {
+      wsum[0][lane] = cc - c0;
+      wsum[1][lane] = aa - a0;
+      wsum[2][lane] = uu - u0;
+    }
+    if (lane == 31) {
+      offsets[E] = cc;
+      *nact = aa;
+      *nunits = uu;
+      s_nunits = uu;
+    }
+  }
+  __syncthreads();
+  {
+    int run = wsum[0][warp] + ci - cs, arun = wsum[1][warp] + ai - as, urun = wsum[2][warp] + ui - us;
+    for (int e = ea; e < eb; ++e) {
+      const int v = cnt[e];
+      cur[e] = run;
+      offsets[e] = run;
+      counts[e] = v;
+      if (v > 0) act[arun++] = e;
+      const int np = (v + kUnitTokens - 1) / kUnitTokens;
+      for (int i = 0; i < np; ++i) {
+        UnitDesc& U = units[urun + i];
+        U.e = e;
+        U.M = min(kUnitTokens, v - i * kUnitTokens);
+        U.pbase = run + i * kUnitTokens;
+        U.pad = 0;
+      }
+      urun += np;
+      run += v;
     }
   }
   __syncthreads();
   for (int r0 = 0; r0 < P; r0 += bd) {
     const int p = r0 + tid;
-    int e = p < P ? __ldcg(idx + p) : -1;
+    int e = p < P ? ld_idx(p) : -1;
     const bool valid = e >= 0 && e < E;
     if (!valid) e = -1;
     const unsigned same = __match_any_sync(0xffffffffu, e);
@@ -217,37 +421,42 @@ __device__ void bucket_block(const int32_t* idx, int P, int k, int E, int32_t* c
         __syncwarp();
         if (valid) {
           perm[base + rank] = p;
+          if (perm_smem) sperm[base + rank] = p;
           if (rank == 0) cur[e] = base + __popc(same);
         }
       }
       __syncthreads();
     }
   }
-  // per-unit pick lists (perm was written by this block above)
+  // per-unit pick lists: one thread per (unit, slot m)
   __threadfence_block();
   __syncthreads();
-  for (int u = tid; u < s_nunits; u += bd) {
+  const int nu = s_nunits;
+  for (int um = tid; um < nu * kUnitTokens; um += bd) {
+    const int u = um / kUnitTokens, m = um % kUnitTokens;
     UnitDesc& U = units[u];
-    const int M = U.M, pb = U.pbase;
-    for (int m = 0; m < kUnitTokens; ++m) {
-      const int p = m < M ? __ldcg(perm + pb + m) : 0;
-      const int t = p / k;
-      U.pick[m] = m < M ? p : -1;
-      U.tok[m] = m < M ? t : 0;
-      U.xs[m] = m < M ? __ldcg(xscale + t) : 0.f;
-      U.w[m] = m < M ? __ldcg(w + p) : 0.f;
-    }
+    const int M = __ldcg(&U.M), pb = __ldcg(&U.pbase);
+    const int p = m < M ? (perm_smem ? sperm[pb + m] : __ldcg(perm + pb + m)) : 0;
+    const int t = p / k;
+    U.pick[m] = m < M ? p : -1;
+    U.tok[m] = m < M ? t : 0;
+    U.xs[m] = m < M ? __ldcg(xscale + t) : 0.f;
+    U.w[m] = m < M ? ld_w(p) : 0.f;
   }
 }
 
 namespace {
 
+__host__ inline size_t fused_select_smem(int E, int P) {
+  return (size_t)(2 * E + 2) * 4 + 256 * 8 + ((size_t)2 * P + 2 * (size_t)E + P) * 4;
+}
+
 __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(RouterArgs a) {
-  extern __shared__ float dsm[];
+  extern __shared__ __align__(16) uint8_t rsm[];
   __shared__ float red[kRouterWarps];
+  __shared__ float half_sum[kRouterWarps * kTokTile];
   __shared__ int last;
-  logits_rows(a);
-  convert_tokens(a, red);
+  logits_and_convert(a, reinterpret_cast<uint16_t*>(rsm), red, half_sum);
   if (!a.fuse_select) return;
   __threadfence();
   __syncthreads();
@@ -255,24 +464,30 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(RouterArgs a)
   __syncthreads();
   if (!last) return;
   __threadfence();
-  const int warp = threadIdx.x >> 5;
-  for (int t = warp; t < a.T; t += kRouterWarps)
-    topk_warp(a.ws.logits + (size_t)t * a.E, a.bias, a.E, a.k, dsm + (size_t)warp * a.E, a.ws.idx + (size_t)t * a.k,
-              a.ws.w + (size_t)t * a.k);
-  __threadfence_block();
-  __syncthreads();
-  bucket_block(a.ws.idx, a.T * a.k, a.k, a.E, a.ws.counts, a.ws.offsets, a.ws.perm, a.ws.act, a.ws.nact,
-               a.ws.units, a.ws.nunits, a.ws.w, a.ws.xscale, reinterpret_cast<int*>(dsm));
+  // shared memory of the last block: [ku: E][sg: E][cand: 256 x 8 bytes][idx: P][w: P][bucketing: 2E + P]
+  const int P = a.T * a.k;
+  uint32_t* ku = reinterpret_cast<uint32_t*>(rsm);
+  float* sg = reinterpret_cast<float*>(ku + a.E);
+  uint2* cand = reinterpret_cast<uint2*>(sg + a.E);  // word offset 2E: 8-byte aligned
+  int32_t* sidx = reinterpret_cast<int32_t*>(cand + 256);
+  float* sw = reinterpret_cast<float*>(sidx + P);
+  int* bsm = reinterpret_cast<int*>(sw + P);
+  for (int t = 0; t < a.T; ++t)
+    topk_block(a.ws.logits + (size_t)t * a.E, a.bias, a.E, a.k, ku, sg, cand, a.ws.idx + (size_t)t * a.k,
+               a.ws.w + (size_t)t * a.k, sidx + (size_t)t * a.k, sw + (size_t)t * a.k);
+  bucket_block(sidx, P, a.k, a.E, a.ws.counts, a.ws.offsets, a.ws.perm, a.ws.act, a.ws.nact, a.ws.units,
+               a.ws.nunits, sw, a.ws.xscale, bsm, true, true);
   if (threadIdx.x == 0) a.ws.sync[0] = 0u;
 }
 
-__global__ void __launch_bounds__(256) topk_kernel(const float* logits, const float* bias, int T, int E, int k,
-                                                   int32_t* idx, float* w) {
-  extern __shared__ float dsm[];
-  const int warp = threadIdx.x >> 5;
-  const int t = blockIdx.x * 8 + warp;
-  if (t >= T) return;
-  topk_warp(logits + (size_t)t * E, bias, E, k, dsm + (size_t)warp * E, idx + (size_t)t * k, w + (size_t)t * k);
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* logits, const float* bias, int T, int E, int k,
+                                                            int32_t* idx, float* w) {
+  extern __shared__ __align__(16) uint8_t tsm[];
+  uint32_t* ku = reinterpret_cast<uint32_t*>(tsm);
+  float* sg = reinterpret_cast<float*>(ku + E);
+  uint2* cand = reinterpret_cast<uint2*>(sg + E);  // word offset 2E: 8-byte aligned
+  for (int t = blockIdx.x; t < T; t += gridDim.x)
+    topk_block(logits + (size_t)t * E, bias, E, k, ku, sg, cand, idx + (size_t)t * k, w + (size_t)t * k);
 }
 
 __global__ void __launch_bounds__(1024) bucket_kernel(const int32_t* idx, int P, int k, int E, int32_t* counts,
@@ -280,20 +495,23 @@ __global__ void __launch_bounds__(1024) bucket_kernel(const int32_t* idx, int P,
                                                       UnitDesc* units, int32_t* nunits, const float* w,
                                                       const float* xscale) {
   extern __shared__ int ism[];
-  bucket_block(idx, P, k, E, counts, offsets, perm, act, nact, units, nunits, w, xscale, ism);
+  bucket_block(idx, P, k, E, counts, offsets, perm, act, nact, units, nunits, w, xscale, ism, false);
 }
 
 }  // namespace
 
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s) {
-  const size_t smem = (size_t)kRouterWarps * a.E * sizeof(float);
+  // dynamic shared memory: the staged token tile, reused by the last block for top-k keys
+  // (kRouterWarps * E floats) and bucketing (2 * E ints)
+  size_t smem = (size_t)kTokTile * a.d * sizeof(uint16_t);
+  if (a.fuse_select) smem = std::max(smem, fused_select_smem(a.E, a.T * a.k));
   static bool attr = false;
   if (!attr) {
     cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     attr = true;
   }
-  const int grid = (a.E + kRouterWarps - 1) / kRouterWarps;
-  router_kernel<<<grid, kRouterWarps * 32, a.fuse_select ? smem : 0, s>>>(a);
+  const int grid = (a.E + kRowsPerCta - 1) / kRowsPerCta;
+  router_kernel<<<grid, kRouterWarps * 32, smem, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -304,7 +522,8 @@ cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, in
     cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     attr = true;
   }
-  topk_kernel<<<(T + 7) / 8, 256, (size_t)8 * E * sizeof(float), s>>>(logits, bias, T, E, k, idx, w);
+  const size_t smem = (size_t)(2 * E + 2) * 4 + 256 * 8;
+  topk_kernel<<<std::min(T, 148 * 8), kTopkThreads, smem, s>>>(logits, bias, T, E, k, idx, w);
   return cudaGetLastError();
 }
 

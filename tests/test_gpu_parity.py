@@ -313,3 +313,14 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     assert np.array_equal(L.forward(x), y_ok)
     k3.k3moe_sync(L.layer)
     L.free()
+
+
+def test_zero_scale_bytes():
+    # E8M0 byte 0 is 2^-127 (a subnormal in fp32): the layer is flagged at pack time and the
+    # kernels take the exact decode for it.
+    d, f, E, k = 256, 256, 8, 2
+    nib, scl = synth.experts(3, 0, 0, E, d, f)
+    scl[:, ::7] = 0
+    L = Small(d, f, E, k, 6, seed=3, nib=nib, scl=scl)
+    _check_layer(L, L.tokens(6), "zero scales")
+    L.free()
