@@ -139,15 +139,15 @@ def _traffic_from_profile(kernel_file: str, summary: str):
 
 # --------------------------------------------------------------------------- b300 arm ---
 
-def build_layer(torch, k3, T_max, bias=None):
+def build_layer(torch, k3, T_max, bias=None, n_exp=E):
     import synth
     nb, sb = synth.expert_bytes(D, F)
-    dn = torch.empty(E * nb, dtype=torch.uint8, device="cuda")
-    ds = torch.empty(E * sb, dtype=torch.uint8, device="cuda")
-    synth.experts_to_device(SEED, 0, 0, E, D, F, dn.data_ptr(), ds.data_ptr())
-    Wr = torch.from_numpy(synth.router_weights(SEED, 0, E, D)).cuda()
+    dn = torch.empty(n_exp * nb, dtype=torch.uint8, device="cuda")
+    ds = torch.empty(n_exp * sb, dtype=torch.uint8, device="cuda")
+    synth.experts_to_device(SEED, 0, 0, n_exp, D, F, dn.data_ptr(), ds.data_ptr())
+    Wr = torch.from_numpy(synth.router_weights(SEED, 0, n_exp, D)).cuda()
     b = None if bias is None else torch.from_numpy(bias).cuda()
-    layer = k3.k3moe_pack_experts(k3.dims(D, F, E, K, T_max), dn, ds, 1, Wr, b)
+    layer = k3.k3moe_pack_experts(k3.dims(D, F, n_exp, K, T_max), dn, ds, 1, Wr, b)
     del dn, ds
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
@@ -169,8 +169,8 @@ def run_b300(args):
         pg = dist
     wl = WORKLOADS[args.workload]
     T = wl["T"]
-    bias = synth.hot_bias(SEED, 0, E, 32, 2.0) if args.workload == "prefill4096" else None
-    layer = build_layer(torch, k3, max(T, 1), bias)
+    bias = synth.hot_bias(SEED, 0, args.experts, 32, 2.0) if args.workload == "prefill4096" else None
+    layer = build_layer(torch, k3, max(T, 1), bias, args.experts)
     calls = args.tokens_per_step if T == 1 else 1
     tokens_per_step = calls * T
     # seeded tokens, distinct per rank
@@ -264,7 +264,9 @@ def run_b300(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "mxfp4 weights -> f16 mma, f32 accumulate",
             "data": "synthetic (seeded splitmix64 experts, N(0,1) bf16 tokens, N(0,1/d) router)",
             "impl": "b300",
-            "config": {"workload": wl["desc"], "calls_per_step": calls, "tokens_per_step": tokens_per_step,
+            "config": {"workload": wl["desc"] + ("" if args.experts == E else
+                                                 f" [profiling case: only {args.experts} experts resident]"),
+                       "calls_per_step": calls, "tokens_per_step": tokens_per_step,
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                        "l2": "inputs larger than L2: 15.7 GB expert pool streamed from HBM; router L2-resident"},
             "weight_gbs": round(weight_bytes_per_step * args.steps * ws / (ms / 1e3) / 1e9, 1),
@@ -369,6 +371,9 @@ def main():
     ap.add_argument("--tokens-per-step", type=int, default=1000)
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--experts", type=int, default=E,
+                    help="experts resident (default 896); fewer gives a small case with the same per-call work "
+                         "at T=1, for profiler captures")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
