@@ -55,6 +55,9 @@ def _L():
         lib.k3o_bucket.argtypes, lib.k3o_bucket.restype = [i32, i32, i32, vp, vp, vp, vp], None
         lib.k3o_expert_ffn.argtypes, lib.k3o_expert_ffn.restype = [i32, i32, vp, vp, vp, vp, vp, vp], None
         lib.k3o_moe.argtypes, lib.k3o_moe.restype = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp], None
+        lib.k3o_bf16_rne.argtypes, lib.k3o_bf16_rne.restype = [ctypes.c_float], ctypes.c_uint16
+        lib.k3o_residual_rmsnorm.argtypes = [i32, i32, vp, vp, d, vp, vp]
+        lib.k3o_residual_rmsnorm.restype = None
         lib.k3o_max_threads.argtypes, lib.k3o_max_threads.restype = [], i32
         lib.k3o_set_threads.argtypes, lib.k3o_set_threads.restype = [i32], None
         _lib = lib
@@ -168,6 +171,22 @@ def layer(x_bits, Wr, bias, k: int, f: int, nib_all, scl_all):
     y, sumabs = moe(x_bits, w, [nib_all[e] for e in flat], [scl_all[e] for e in flat], f)
     return dict(idx=idx, w=w, logits=logits, keys=keys, counts=counts, offsets=offsets, perm=perm, y=y,
                 sumabs=sumabs)
+
+
+def bf16_rne(v: float) -> int:
+    """float32 value -> bf16 bit pattern, round to nearest, ties to even."""
+    return int(_L().k3o_bf16_rne(v))
+
+
+def residual_rmsnorm(y, x_bits, eps: float):
+    """Glue between stacked layers: -> (x_next uint16[T,d], x_norm uint16[T,d]) as bf16 bits."""
+    y, x_bits = _c(y, np.float32), _c(x_bits, np.uint16)
+    T, dd = x_bits.shape
+    assert y.shape == (T, dd)
+    x_next = np.empty((T, dd), np.uint16)
+    x_norm = np.empty((T, dd), np.uint16)
+    _L().k3o_residual_rmsnorm(T, dd, _p(y), _p(x_bits), eps, _p(x_next), _p(x_norm))
+    return x_next, x_norm
 
 
 def max_threads() -> int:

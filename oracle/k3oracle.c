@@ -20,6 +20,9 @@
  *          unbiased scores.
  *   [GL]   same page, glossary: MoE picks 16 of 896 experts per layer; MXFP4 is
  *          0.53125 bytes per parameter.
+ *   [EX]   same page, "what you learn", the exercise paragraph: the engine has an
+ *          RMSNorm kernel with an epsilon (used here only as glue between stacked
+ *          layers, see k3o_residual_rmsnorm).
  * Where the pages are silent the code says READING and states the reading taken.
  *
  * Canonical expert layout (the input format of the library, defined by us):
@@ -235,6 +238,44 @@ void k3o_moe(int T, int d, int f, int k, const uint16_t* x, const double* w, con
     }
   free(o);
   free(a);
+}
+
+/* ------------------------------------------------- glue between layers ---- */
+
+/* Round a float to bf16, to nearest with ties to even, by its definition: keep the upper
+ * 16 bits of the binary32 pattern, adding one unit of the kept part when the dropped 16
+ * bits exceed half a unit, or equal half a unit and the kept part is odd.  NaN stays NaN. */
+uint16_t k3o_bf16_rne(float v) {
+  uint32_t u;
+  memcpy(&u, &v, 4);
+  if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu)) return (uint16_t)((u >> 16) | 0x40);
+  uint32_t keep = u >> 16, drop = u & 0xffffu;
+  if (drop > 0x8000u || (drop == 0x8000u && (keep & 1u))) keep += 1;
+  return (uint16_t)keep;
+}
+
+/* Residual and pre-norm between stacked layers (the layer's output excludes the residual).
+ * READING: the stacked-layer workload adds each layer's output to its input,
+ *   x_next = bf16_rne(x + y), the sum taken in binary32 (the precision the kernel rounds
+ *   from; the result is an integer code, so both sides decide it in the same precision);
+ * and, as a transformer block does before its MoE ([EX] names the engine's RMSNorm), feeds
+ * the next layer the weightless RMSNorm of x_next:
+ *   x_norm = bf16_rne( x_next / sqrt( (1/d) * sum_j x_next_j^2 + eps ) ), in fp64. */
+void k3o_residual_rmsnorm(int T, int d, const float* y, const uint16_t* x, double eps, uint16_t* x_next,
+                          uint16_t* x_norm) {
+  for (int t = 0; t < T; ++t) {
+    double ss = 0.0;
+    for (int j = 0; j < d; ++j) {
+      const float sum = (float)k3o_bf16(x[(size_t)t * d + j]) + y[(size_t)t * d + j];
+      const uint16_t r = k3o_bf16_rne(sum);
+      x_next[(size_t)t * d + j] = r;
+      const double rv = k3o_bf16(r);
+      ss += rv * rv;
+    }
+    const double inv = 1.0 / sqrt(ss / d + eps);
+    for (int j = 0; j < d; ++j)
+      x_norm[(size_t)t * d + j] = k3o_bf16_rne((float)(k3o_bf16(x_next[(size_t)t * d + j]) * inv));
+  }
 }
 
 /* ---------------------------------------------------------------- threads ---- */

@@ -298,3 +298,71 @@ def test_layer_k1_combine_is_identity():
     for t in range(3):
         _, o, _ = oracle.expert_ffn(d, f, nib[out["idx"][t, 0]], scl[out["idx"][t, 0]], xf[t])
         assert np.array_equal(out["y"][t], o)
+
+
+# ------------------------------------------------------ glue between layers ---
+
+def _torch_bf16_bits(v: np.ndarray) -> np.ndarray:
+    torch = pytest.importorskip("torch")
+    t = torch.from_numpy(np.ascontiguousarray(v, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def test_bf16_rne_hand_values():
+    # ulp(1) in bf16 is 2^-7: 1 + 2^-8 is a tie (stays at the even code 1.0), 1 + 3*2^-8 is a
+    # tie between 1 + 2^-7 (odd) and 1 + 2^-6 (even), a hair above a tie rounds up.
+    assert oracle.bf16_rne(1.0) == 0x3F80
+    assert oracle.bf16_rne(1.0 + 2 ** -8) == 0x3F80
+    assert oracle.bf16_rne(1.0 + 3 * 2 ** -8) == 0x3F82
+    assert oracle.bf16_rne(1.0 + 2 ** -8 + 2 ** -20) == 0x3F81
+    assert oracle.bf16_rne(-1.5) == 0xBFC0
+    assert oracle.bf16_rne(float("inf")) == 0x7F80
+    assert oracle.bf16_rne(3.4e38) == 0x7F80  # above the largest finite bf16: rounds to inf
+
+
+def test_bf16_rne_matches_library_conversion():
+    # a second formulation: torch's float32 -> bfloat16 conversion (round to nearest even)
+    rng = np.random.default_rng(3)
+    with np.errstate(over="ignore", invalid="ignore"):
+        wide = (rng.standard_normal(4000) * 10.0 ** rng.integers(-30, 30, 4000)).astype(np.float32)
+    bits = rng.integers(0, 2 ** 32, 4000, dtype=np.uint64).astype(np.uint32).view(np.float32)
+    v = np.concatenate([wide, bits])
+    v = v[np.isfinite(v)]
+    ref = _torch_bf16_bits(v)
+    got = np.array([oracle.bf16_rne(float(a)) for a in v], np.uint16)
+    assert np.array_equal(got, ref)
+
+
+def test_residual_is_bf16_of_the_fp32_sum():
+    rng = np.random.default_rng(4)
+    T, d = 3, 96
+    x = synth.tokens_bf16(4, 0, 0, T, d)
+    y = (rng.standard_normal((T, d)) * 50).astype(np.float32)
+    x_next, _ = oracle.residual_rmsnorm(y, x, 1e-6)
+    ref = _torch_bf16_bits(synth.bf16_bits_to_f32(x) + y)
+    assert np.array_equal(x_next, ref)
+
+
+def test_rmsnorm_closed_forms():
+    d = 4
+    x = np.zeros((2, d), np.uint16)
+    # (3, 4, 0, 0): mean square 25/4, root 2.5 -> (1.2, 1.6, 0, 0); constant -7 -> all -1
+    y = np.array([[3, 4, 0, 0], [-7, -7, -7, -7]], np.float32)
+    _, xn = oracle.residual_rmsnorm(y, x, 0.0)
+    assert np.array_equal(xn[0], _torch_bf16_bits(np.array([1.2, 1.6, 0, 0], np.float32)))
+    assert np.array_equal(xn[1], np.full(d, 0xBF80, np.uint16))
+    # eps enters under the root: (1,1,1,1) with eps = 3 -> 1/2
+    _, xn = oracle.residual_rmsnorm(np.ones((1, d), np.float32), np.zeros((1, d), np.uint16), 3.0)
+    assert np.array_equal(xn[0], np.full(d, 0x3F00, np.uint16))
+
+
+def test_rmsnorm_scale_invariance_and_unit_rms():
+    rng = np.random.default_rng(5)
+    d = 512
+    y = rng.standard_normal((1, d)).astype(np.float32)
+    z = np.zeros((1, d), np.uint16)
+    _, a = oracle.residual_rmsnorm(y, z, 0.0)
+    _, b = oracle.residual_rmsnorm(y * np.float32(2.0 ** 40), z, 0.0)
+    assert np.array_equal(a, b)
+    v = synth.bf16_bits_to_f32(a).astype(np.float64)
+    assert abs(np.mean(v * v) - 1.0) < 2 * 2 ** -8
