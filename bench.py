@@ -46,6 +46,9 @@ WORKLOADS = {
     "decode1": dict(T=1, desc="K3 MoE layer, single-token decode: d=7168 f=1536 E=896 k=16, T=1 per call"),
     "decode64": dict(T=64, desc="K3 MoE layer, batched decode: d=7168 f=1536 E=896 k=16, T=64 per call"),
     "prefill4096": dict(T=4096, desc="K3 MoE layer, prefill: d=7168 f=1536 E=896 k=16, T=4096, +2.0 bias on 32 experts"),
+    "stack4": dict(T=1, desc="4 stacked K3 MoE layers (d=7168 f=1536 E=896 k=16; between them r=bf16(r+y), "
+                             "next input RMSNorm(r)), "
+                             "T=1 decode, 62.9 GB expert pool in pinned host memory behind a device LRU cache"),
 }
 
 
@@ -233,7 +236,9 @@ def run_b300(args):
     gu_bytes_per_launch = (distinct / calls) * GATEUP_BYTES
     achieved = gu_bytes_per_launch / (gu_ms / gu_n / 1e3) / 1e9 if gu_n else None
     launches = sum(v[1] for v in prof.values())
-    traffic = _traffic_from_profile("mxfp4_routed_expert_06_b300/csrc/decode_ffn.cu", "gateup_decode_k3_t1.txt")
+    # the committed capture is of a T=1 launch; other workloads have no capture of their own
+    traffic = (_traffic_from_profile("mxfp4_routed_expert_06_b300/csrc/decode_ffn.cu", "gateup_decode_k3_t1.txt")
+               if T == 1 else None)
 
     # end to end through the public host-buffer entry point
     xh = torch.from_numpy(xs.view(np.int16)).pin_memory()
@@ -286,6 +291,126 @@ def run_b300(args):
             "cpu_baseline": cpu,
         }
     k3.k3moe_layer_free(layer)
+    if pg:
+        pg.destroy_process_group()
+    return out
+
+
+def run_stack4(args):
+    """Four stacked layers in cache mode: a step is tokens_per_step T=1 tokens, each through all
+    four layers (the caller's residual between them); the budget sets the device cache size."""
+    import torch
+    import synth
+    import mxfp4_routed_expert_06_b300 as k3
+
+    ws, rank = _dist()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        pg = dist
+    n_layers = 4
+    budget = int(args.budget_gb * 1e9)
+    cache = k3.k3moe_cache_create(budget, EXPERT_BYTES)
+    nb, sb = synth.expert_bytes(D, F)
+    layers = []
+    for l in range(n_layers):
+        dn = torch.empty(E * nb, dtype=torch.uint8, device="cuda")
+        ds = torch.empty(E * sb, dtype=torch.uint8, device="cuda")
+        synth.experts_to_device(SEED, l, 0, E, D, F, dn.data_ptr(), ds.data_ptr())
+        Wr = torch.from_numpy(synth.router_weights(SEED, l, E, D)).cuda()
+        layers.append(k3.k3moe_pack_experts(k3.dims(D, F, E, K, 1), dn, ds, 1, Wr, None, cache))
+        del dn, ds, Wr
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    n_tok = args.tokens_per_step
+    xs = synth.tokens_bf16(SEED, 0, rank * 10_000_000, n_tok, D)
+    xd = torch.from_numpy(xs.view(np.int16)).cuda()
+    ys = torch.empty((n_tok, n_layers, D), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    resid = torch.empty((1, D), dtype=torch.int16, device="cuda")
+    xin = torch.empty((1, D), dtype=torch.int16, device="cuda")
+
+    def step():
+        # layer 0 takes the token; then r = bf16(r + y) and the next layer takes RMSNorm(r)
+        for t in range(n_tok):
+            x = xd[t:t + 1]
+            resid.copy_(x)
+            for l, L in enumerate(layers):
+                y = ys[t, l:l + 1]
+                k3.k3moe_layer_forward(L, x, 1, y, stream)
+                k3.k3moe_residual_rmsnorm(y, resid, 1, D, 1e-6, resid, xin, stream)
+                x = xin
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    k3.k3moe_cache_reset_stats(cache)
+    for L in layers:
+        k3.k3moe_profile(L, True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    ms = e0.elapsed_time(e1)
+    clk = clocks.stop()
+    st = k3.k3moe_cache_stats(cache)
+    prof = {}
+    for L in layers:
+        for kname, (kms, kn) in k3.k3moe_profile_read(L).items():
+            a = prof.setdefault(kname, [0.0, 0])
+            a[0] += kms
+            a[1] += kn
+        k3.k3moe_profile(L, False)
+    if pg:
+        t = torch.tensor([ms], device="cuda")
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    value = n_tok * args.steps * ws / (ms / 1e3)
+    hbm_peak, _, peak_kind = _peaks()
+    gu_ms, gu_n = prof.get("gateup", (0.0, 0))
+    achieved = K * GATEUP_BYTES / (gu_ms / gu_n / 1e3) / 1e9 if gu_n else None
+    out = None
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "mxfp4 weights -> f16 mma, f32 accumulate",
+            "data": "synthetic (seeded splitmix64 experts, N(0,1) bf16 tokens, N(0,1/d) router)",
+            "impl": "b300",
+            "config": {"workload": WORKLOADS["stack4"]["desc"], "budget_gb": args.budget_gb,
+                       "cache_slots": budget // EXPERT_BYTES, "tokens_per_step": n_tok, "layers": n_layers,
+                       "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                       "l2": "inputs larger than L2: 62.9 GB pool"},
+            "cache": {"hits": st["hits"], "misses": st["misses"], "evictions": st["evictions"],
+                      "hit_rate": round(st["hits"] / max(1, st["hits"] + st["misses"]), 4),
+                      "h2d_gb": round(st["h2d_bytes"] / 1e9, 3),
+                      "h2d_gbs_of_copy_time": round(st["h2d_bytes"] / 1e6 / max(st["h2d_ms"], 1e-9), 2),
+                      "h2d_gbs_of_wall": round(st["h2d_bytes"] / 1e6 / ms, 2)},
+            "roofline": {"bound": "hbm", "kernel": "gateup_kernel (gate/up + SwiGLU, register decode)",
+                         "achieved": None if achieved is None else round(achieved, 1), "peak": hbm_peak,
+                         "unit": "GB/s", "frac": None if achieved is None else round(achieved / hbm_peak, 4),
+                         "peak_kind": f"{peak_kind} (HBM copy peak)", "traffic": None},
+            "kernel_ms_per_launch": {k: round(v[0] / v[1], 5) for k, v in prof.items() if v[1]},
+            "gpu_launches": int(sum(v[1] for v in prof.values())),
+            "clocks": clk,
+            "cpu_baseline": None,
+        }
+    for L in layers:
+        k3.k3moe_layer_free(L)
+    k3.k3moe_cache_destroy(cache)
     if pg:
         pg.destroy_process_group()
     return out
@@ -368,7 +493,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="b300", choices=["b300", "reference"])
     ap.add_argument("--workload", default="decode1", choices=sorted(WORKLOADS))
-    ap.add_argument("--tokens-per-step", type=int, default=1000)
+    ap.add_argument("--tokens-per-step", type=int, default=None,
+                    help="T=1 calls per step (default 1000; 256 for stack4)")
+    ap.add_argument("--budget-gb", type=float, default=8.0, help="stack4: device cache budget (1 GB = 1e9 B)")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--experts", type=int, default=E,
@@ -377,7 +504,14 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    out = run_reference(args) if args.impl == "reference" else run_b300(args)
+    if args.tokens_per_step is None:
+        args.tokens_per_step = 256 if args.workload == "stack4" else 1000
+    if args.impl == "reference":
+        out = run_reference(args)
+    elif args.workload == "stack4":
+        out = run_stack4(args)
+    else:
+        out = run_b300(args)
     if out is not None:
         print(json.dumps(out), flush=True)
 

@@ -226,8 +226,29 @@ void k3moe_layer_free(k3moe_layer* layer);
 int k3moe_cache_create(size_t budget_bytes, size_t slot_bytes, k3moe_cache** out);
 int k3moe_cache_stats(const k3moe_cache* cache, k3moe_cache_stats_t* out);
 int k3moe_cache_reset_stats(k3moe_cache* cache);
-/* Destroy after every layer that uses it has been freed. */
+/* Destroy after every layer that uses it has been freed or moved to another cache. */
 void k3moe_cache_destroy(k3moe_cache* cache);
+/* Moves a layer packed in cache mode (its experts in a pinned host pool) to another cache
+ * with the same slot_bytes, e.g. to run the same layers under a different memory budget.
+ * Waits for the layer's last stream, then drops the layer's experts from its old cache (its
+ * next call misses on every expert).  The output of later calls is unchanged: the budget
+ * changes only which copies run.  Errors: INVALID_ARG (NULL, a layer packed without a cache,
+ * or slot_bytes differ), CUDA. */
+int k3moe_layer_set_cache(k3moe_layer* layer, k3moe_cache* cache);
+
+/* Glue between stacked layers (the layer's y excludes any residual).  For T tokens of
+ * width d:  x_next = bf16_rne(x + y), the sum in fp32;  x_norm = bf16_rne(x_next /
+ * sqrt(mean_j(x_next_j^2) + eps)), a weightless RMSNorm, the input a pre-norm block feeds
+ * its next MoE layer.  The pages print no formula for it: the kimi-k3-in-c deep dive ("what
+ * you learn", exercise paragraph) names the engine's RMSNorm kernel and its epsilon.
+ *   y       device fp32 [T][d]                     (read)
+ *   x       device bf16 bits [T][d]                (read; may alias x_next or x_norm)
+ *   x_next  device bf16 bits [T][d]                (written)
+ *   x_norm  device bf16 bits [T][d]                (written; must not alias x_next or y)
+ * Asynchronous on `stream`.  Errors: INVALID_ARG (NULL, T < 1, d < 1 or d > 65536, eps < 0
+ * or not finite, x_norm aliasing x_next), CUDA.  Non-finite sums propagate. */
+int k3moe_residual_rmsnorm(const float* y, const void* x, int T, int d, float eps, void* x_next, void* x_norm,
+                           void* stream);
 
 const char* k3moe_last_error(void);
 

@@ -74,6 +74,8 @@ _SIGS = {
     "k3moe_cache_stats": ([_vp, ctypes.POINTER(k3moe_cache_stats_t)], _i),
     "k3moe_cache_reset_stats": ([_vp], _i),
     "k3moe_cache_destroy": ([_vp], None),
+    "k3moe_layer_set_cache": ([_vp, _vp], _i),
+    "k3moe_residual_rmsnorm": ([_vp, _vp, _i, _i, ctypes.c_float, _vp, _vp, _vp], _i),
     "k3moe_last_error": ([], ctypes.c_char_p),
     "k3moe_router_topk_noalloc": ([_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp], _i),
 }
@@ -219,3 +221,11 @@ def k3moe_cache_reset_stats(cache) -> None:
 
 def k3moe_cache_destroy(cache) -> None:
     _lib.k3moe_cache_destroy(_handle(cache))
+
+
+def k3moe_residual_rmsnorm(y, x, T: int, d: int, eps: float, x_next, x_norm, stream=None) -> None:
+    _check(_lib.k3moe_residual_rmsnorm(_ptr(y), _ptr(x), T, d, eps, _ptr(x_next), _ptr(x_norm), _stream(stream)))
+
+
+def k3moe_layer_set_cache(layer, cache) -> None:
+    _check(_lib.k3moe_layer_set_cache(_handle(layer), _handle(cache)))

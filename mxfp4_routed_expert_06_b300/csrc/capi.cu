@@ -6,6 +6,7 @@
 #include <list>
 #include <unordered_map>
 #include <utility>
+#include <cmath>
 #include <vector>
 
 #include "k3moe_internal.cuh"
@@ -172,6 +173,23 @@ int alloc_workspace(k3moe_layer* L) {
   return K3MOE_OK;
 }
 
+// Drops the layer's experts from its cache: their slots become free (least recently used).
+void detach_cache(k3moe_layer* L) {
+  k3moe_cache* C = L->cache;
+  if (!C) return;
+  for (int s = 0; s < C->n_slots; ++s) {
+    if (C->slot_key[s] >= 0 && (int)(C->slot_key[s] >> 32) == L->uid) {
+      C->where.erase(C->slot_key[s]);
+      C->slot_key[s] = -1;
+      C->lru.erase(C->lru_pos[s]);
+      C->lru.push_back(s);
+      C->lru_pos[s] = std::prev(C->lru.end());
+    }
+  }
+  C->users -= 1;
+  L->cache = nullptr;
+}
+
 void free_layer(k3moe_layer* L) {
   if (!L) return;
   if (L->last_stream) cudaStreamSynchronize(L->last_stream);
@@ -191,17 +209,7 @@ void free_layer(k3moe_layer* L) {
   }
   for (auto e : L->spare_events) cudaEventDestroy(e);
   if (L->copies_done) cudaEventDestroy(L->copies_done);
-  if (L->cache) {
-    // drop this layer's experts from the cache
-    k3moe_cache* C = L->cache;
-    for (int s = 0; s < C->n_slots; ++s) {
-      if (C->slot_key[s] >= 0 && (int)(C->slot_key[s] >> 32) == L->uid) {
-        C->where.erase(C->slot_key[s]);
-        C->slot_key[s] = -1;
-      }
-    }
-    C->users -= 1;
-  }
+  detach_cache(L);
   delete L;
 }
 
@@ -530,6 +538,33 @@ int k3moe_pack_experts(const k3moe_dims* dims, const void* canon_nib, const void
 }
 
 void k3moe_layer_free(k3moe_layer* L) { free_layer(L); }
+
+int k3moe_residual_rmsnorm(const float* y, const void* x, int T, int d, float eps, void* x_next, void* x_norm,
+                           void* stream) {
+  if (!y || !x || !x_next || !x_norm) return fail(K3MOE_ERR_INVALID_ARG, "NULL argument");
+  if (T < 1 || d < 1 || d > 65536) return fail(K3MOE_ERR_INVALID_ARG, "T=%d, d=%d out of range", T, d);
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(K3MOE_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  if (x_norm == x_next) return fail(K3MOE_ERR_INVALID_ARG, "x_norm must not alias x_next");
+  CUDA_TRY(launch_residual_rmsnorm(y, reinterpret_cast<const uint16_t*>(x), T, d, eps,
+                                   reinterpret_cast<uint16_t*>(x_next), reinterpret_cast<uint16_t*>(x_norm),
+                                   reinterpret_cast<cudaStream_t>(stream)));
+  return K3MOE_OK;
+}
+
+int k3moe_layer_set_cache(k3moe_layer* L, k3moe_cache* C) {
+  if (!L || !C) return fail(K3MOE_ERR_INVALID_ARG, "NULL argument");
+  if (!L->pool) return fail(K3MOE_ERR_INVALID_ARG, "layer was packed without a cache (its experts live on the device)");
+  if (C->slot_bytes != L->exp_bytes)
+    return fail(K3MOE_ERR_INVALID_ARG, "cache slot_bytes %zu != packed expert bytes %zu", C->slot_bytes, L->exp_bytes);
+  if (C == L->cache) return K3MOE_OK;
+  if (L->last_stream) CUDA_TRY(cudaStreamSynchronize(L->last_stream));
+  if (L->cache) CUDA_TRY(cudaStreamSynchronize(L->cache->copy_stream));
+  detach_cache(L);
+  L->cache = C;
+  L->uid = C->next_uid++;
+  C->users += 1;
+  return K3MOE_OK;
+}
 
 int k3moe_router_topk(k3moe_layer* L, const void* x, int T, int32_t* idx, float* w, void* stream) {
   if (!L || !x || !idx || !w) return fail(K3MOE_ERR_INVALID_ARG, "NULL argument");

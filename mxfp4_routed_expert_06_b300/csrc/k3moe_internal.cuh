@@ -132,6 +132,8 @@ struct FfnArgs {
 cudaError_t launch_gateup(const FfnArgs& a, cudaStream_t s);
 cudaError_t launch_down(const FfnArgs& a, cudaStream_t s);
 cudaError_t launch_combine(const FfnArgs& a, cudaStream_t s);
+cudaError_t launch_residual_rmsnorm(const float* y, const uint16_t* x, int T, int d, float eps, uint16_t* x_next,
+                                    uint16_t* x_norm, cudaStream_t s);
 
 // canon_nib/canon_scl point at the canonical bytes of the first of n_exp experts; dst at its packed block.
 cudaError_t launch_pack(const uint8_t* canon_nib, const uint8_t* canon_scl, int n_exp, int d, int f, uint8_t* dst,

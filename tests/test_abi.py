@@ -70,7 +70,13 @@ def test_bad_arguments_are_refused_without_device_work():
     assert ei.value.code == k3.K3MOE_ERR_INVALID_ARG
     for fn, args in [(k3.k3moe_layer_forward, (None, 1, 1, 1)), (k3.k3moe_router_topk, (None, 1, 1, 1, 1)),
                      (k3.k3moe_bucket, (None, 1, 1, 1, 1, 1)), (k3.k3moe_set_option, (None, 1, 0)),
-                     (k3.k3moe_profile, (None, 1))]:
+                     (k3.k3moe_profile, (None, 1)), (k3.k3moe_layer_set_cache, (None, 1)),
+                     (k3.k3moe_residual_rmsnorm, (None, 16, 1, 8, 0.0, 32, 48)),
+                     (k3.k3moe_residual_rmsnorm, (16, 32, 0, 8, 0.0, 48, 64)),
+                     (k3.k3moe_residual_rmsnorm, (16, 32, 1, 70000, 0.0, 48, 64)),
+                     (k3.k3moe_residual_rmsnorm, (16, 32, 1, 8, -1.0, 48, 64)),
+                     (k3.k3moe_residual_rmsnorm, (16, 32, 1, 8, float("nan"), 48, 64)),
+                     (k3.k3moe_residual_rmsnorm, (16, 32, 1, 8, 0.0, 48, 48))]:
         with pytest.raises(k3.K3MoEError) as ei:
             fn(*args)
         assert ei.value.code == k3.K3MOE_ERR_INVALID_ARG
