@@ -108,6 +108,7 @@ struct k3moe_layer {
   int test_stall = 0;                           // next forward stalls its FFN consumers (timeout test)
   int ring_depth = 0;                           // 0: automatic
   bool zero_scales = false;                     // some E8M0 scale byte is 0 (2^-127, a subnormal)
+  int s_min = 255, s_max = 0;                   // range of the layer's scale bytes
 };
 
 namespace {
@@ -156,7 +157,9 @@ int alloc_workspace(k3moe_layer* L) {
       {(void**)&w.nact, 4},              {(void**)&w.units, (P / kUnitTokens + D.E + 1) * sizeof(UnitDesc)},
       {(void**)&w.nunits, 4},            {(void**)&w.hbuf, P * D.f * 4},        {(void**)&w.pair, P * (D.f / 32) * 4},
       {(void**)&w.hfrag, P * D.f * 2},   {(void**)&w.hscale, P * (D.f / 32) * 4},
-      {(void**)&w.obuf, P * D.d * 4},    {(void**)&w.sync, 64},                 {(void**)&w.bad, 4},
+      {(void**)&w.obuf, P * D.d * 4},    {(void**)&w.sync, 64},                 {(void**)&w.bad, 16},
+      {(void**)&w.hmax, P * 4},          {(void**)&w.mtiles, (P / 128 + D.E + 1) * sizeof(int4)},
+      {(void**)&w.nmtiles, 4},
   };
   size_t total = 0;
   for (auto& it : items) total += align256(it.bytes);
@@ -226,7 +229,7 @@ cudaError_t reset_after_timeout(k3moe_layer* L) {
 bool use_gemm(const k3moe_layer* L, int T) {
   if (L->path == K3MOE_PATH_GEMM) return true;
   if (L->path == K3MOE_PATH_DECODE) return false;
-  return (long long)T >= L->gemm_min_t;
+  return (long long)T >= L->gemm_min_t && gemm_scales_ok(L->s_min, L->s_max);
 }
 
 // Router + selection + bucketing into the workspace.
@@ -314,10 +317,64 @@ int make_resident(k3moe_layer* L, cudaStream_t s) {
   return K3MOE_OK;
 }
 
+// Large T: the tcgen05 grouped GEMM path (gemm_tc.cu), then the slot-ordered combine.
+int forward_gemm(k3moe_layer* L, const void* x, int T, float* y, cudaStream_t s) {
+  const k3moe_dims& D = L->dims;
+  int rc = run_routing(L, x, T, s);
+  if (rc) return rc;
+  if (L->cache) {
+    rc = make_resident(L, s);
+    if (rc) return rc;
+  }
+  Workspace& w = L->ws;
+  const int P = T * D.k;
+  GemmFfn q{};
+  q.expert_ptr = L->eptr_dev;
+  q.d = D.d;
+  q.f = D.f;
+  q.k = D.k;
+  q.T = T;
+  q.s_ref = L->s_max - 13;
+  q.wscale = std::ldexp(1.0f, q.s_ref - 127);
+  q.mtiles = w.mtiles;
+  q.nmtiles = w.nmtiles;
+  q.perm = w.perm;
+  q.w = w.w;
+  q.xs = w.xscale;
+  q.xg = reinterpret_cast<__half*>(w.obuf);
+  q.hbuf = w.hbuf;
+  q.hmax = w.hmax;
+  q.h16 = w.hfrag;
+  q.hs = w.hscale;
+  q.obuf = w.obuf;
+  q.err = w.sync + 1;
+  q.wait_ns = L->wait_ns;
+  q.num_sms = L->num_sms;
+  rc = timed_launch(L, KID_GATHER, s, [&] {
+    cudaError_t e = launch_gemm_prep(q, reinterpret_cast<const uint16_t*>(x), w.counts, w.offsets, D.E, s);
+    return e == cudaSuccess ? cudaMemsetAsync(w.hmax, 0, (size_t)P * 4, s) : e;
+  });
+  if (rc) return rc;
+  rc = timed_launch(L, KID_GEMM_GU, s, [&] { return launch_gemm_gu(q, s); });
+  if (rc) return rc;
+  rc = timed_launch(L, KID_GATHER, s, [&] { return launch_gemm_h16(q, P, s); });
+  if (rc) return rc;
+  rc = timed_launch(L, KID_GEMM_DN, s, [&] { return launch_gemm_dn(q, s); });
+  if (rc) return rc;
+  FfnArgs fa{L->eptr_dev, D.d, D.f, D.E, D.k, T, L->ws, y, L->num_sms, L->wait_ns, 0, 0, 0};
+  return timed_launch(L, KID_COMBINE, s, [&] { return launch_combine(fa, s); });
+}
+
 int forward_impl(k3moe_layer* L, const void* x, int T, float* y, cudaStream_t s) {
   const k3moe_dims& D = L->dims;
   L->last_stream = s;
-  if (use_gemm(L, T)) return fail(K3MOE_ERR_UNSUPPORTED, "grouped-GEMM path is not built yet");
+  if (use_gemm(L, T)) {
+    if (!gemm_scales_ok(L->s_min, L->s_max))
+      return fail(K3MOE_ERR_UNSUPPORTED,
+                  "scale bytes span %d..%d: wider than the 36 steps the fp16 tensor-core path holds exactly",
+                  L->s_min, L->s_max);
+    return forward_gemm(L, x, T, y, s);
+  }
   int rc = run_routing(L, x, T, s);
   if (rc) return rc;
   if (L->cache) {
@@ -491,6 +548,11 @@ int k3moe_pack_experts(const k3moe_dims* dims, const void* canon_nib, const void
     }
     memset((void*)L->eptr_host, 0, (size_t)D.E * sizeof(void*));
   }
+  {
+    const int32_t init[4] = {0, 255, 0, 0};  // flags, min scale byte, max scale byte
+    ok = cudaMemcpyAsync(L->ws.bad, init, sizeof(init), cudaMemcpyHostToDevice, s) == cudaSuccess &&
+         cudaStreamSynchronize(s) == cudaSuccess;
+  }
   for (int e0 = 0; e0 < D.E && ok; e0 += chunk) {
     const int n = std::min(chunk, D.E - e0);
     const uint8_t* src_n;
@@ -513,15 +575,18 @@ int k3moe_pack_experts(const k3moe_dims* dims, const void* canon_nib, const void
            cudaSuccess;
     if (ok && !src_on_device) ok = cudaStreamSynchronize(s) == cudaSuccess;  // staging reused next chunk
   }
-  int32_t bad = 0;
-  if (ok) ok = cudaMemcpyAsync(&bad, L->ws.bad, 4, cudaMemcpyDeviceToHost, s) == cudaSuccess;
+  int32_t flags[4] = {0, 255, 0, 0};
+  if (ok) ok = cudaMemcpyAsync(flags, L->ws.bad, sizeof(flags), cudaMemcpyDeviceToHost, s) == cudaSuccess;
   if (ok) ok = cudaStreamSynchronize(s) == cudaSuccess;
   cudaFree(stage_nib);
   cudaFree(stage_scl);
   cudaFree(stage_out);
   if (!ok) return bail(fail(K3MOE_ERR_CUDA, "packing failed: %s", cudaGetErrorString(cudaGetLastError())));
+  const int32_t bad = flags[0];
   if (bad & 1) return bail(fail(K3MOE_ERR_INVALID_ARG, "a scale byte is 255 (E8M0 NaN)"));
   L->zero_scales = (bad & 2) != 0;
+  L->s_min = flags[1];
+  L->s_max = flags[2];
   if (!cache) {
     std::vector<const uint8_t*> ptrs(D.E);
     for (int e = 0; e < D.E; ++e) ptrs[e] = L->packed + (size_t)e * eb;

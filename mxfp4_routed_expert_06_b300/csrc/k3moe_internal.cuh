@@ -83,7 +83,13 @@ struct Workspace {
   float* hscale = nullptr;      // [P][f/32] power of two per (pick, 32-block)
   float* obuf = nullptr;        // [P][d] w-scaled expert outputs
   uint32_t* sync = nullptr;     // [16]: [0] router last-block ticket, [1] device error flags
-  int32_t* bad = nullptr;       // [1] pack-time error flag
+  int32_t* bad = nullptr;       // [4] pack time: [0] error flags, [1] min scale byte, [2] max scale byte
+  // tensor-core path (large T); it also reuses obuf (first as xg, the fp16 rows of x in bucketed
+  // order [P][d], which the down projection then overwrites), hbuf (fp32 h [P][f]), hfrag (as
+  // h16 [P][f]) and hscale (as the per-row power of two of h16), xscale (per-token power of two)
+  uint32_t* hmax = nullptr;     // [P] float bits of max |h| per bucketed row
+  int4* mtiles = nullptr;       // [P/128 + E] {expert, first bucketed row, rows, 0}
+  int32_t* nmtiles = nullptr;   // [1]
 };
 
 enum KernelId {
@@ -132,6 +138,33 @@ struct FfnArgs {
 cudaError_t launch_gateup(const FfnArgs& a, cudaStream_t s);
 cudaError_t launch_down(const FfnArgs& a, cudaStream_t s);
 cudaError_t launch_combine(const FfnArgs& a, cudaStream_t s);
+// Tensor-core grouped GEMM path (gemm_tc.cu).
+struct GemmFfn {
+  const uint8_t* const* expert_ptr;
+  int d, f, k, T;
+  int s_ref;                 // weights enter fp16 as e2m1 * 2^(s - s_ref)
+  float wscale;              // 2^(s_ref - 127)
+  const int4* mtiles;
+  const int32_t* nmtiles;
+  const int32_t* perm;
+  const float* w;            // [P] combine weights by pick
+  float* xs;                 // [T] power of two per token
+  __half* xg;                // [P][d] fp16 image of x, rows in bucketed order
+  float* hbuf;               // [P][f]
+  uint32_t* hmax;            // [P]
+  __half* h16;               // [P][f]
+  float* hs;                 // [P]
+  float* obuf;               // [P][d]
+  uint32_t* err;
+  unsigned long long wait_ns;
+  int num_sms;
+};
+bool gemm_scales_ok(int s_min, int s_max);
+cudaError_t launch_gemm_prep(const GemmFfn& q, const uint16_t* x, const int32_t* counts, const int32_t* offsets,
+                             int E, cudaStream_t s);
+cudaError_t launch_gemm_gu(const GemmFfn& q, cudaStream_t s);
+cudaError_t launch_gemm_h16(const GemmFfn& q, int P, cudaStream_t s);
+cudaError_t launch_gemm_dn(const GemmFfn& q, cudaStream_t s);
 cudaError_t launch_residual_rmsnorm(const float* y, const uint16_t* x, int T, int d, float eps, uint16_t* x_next,
                                     uint16_t* x_norm, cudaStream_t s);
 

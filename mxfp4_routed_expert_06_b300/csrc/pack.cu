@@ -24,6 +24,7 @@ __global__ void pack_kernel(const uint8_t* __restrict__ canon_nib, const uint8_t
   const size_t can_nib = 3ull * f * d / 2, can_scl = 3ull * f * d / 32;
   const size_t mat_nib = (size_t)f * d / 2, mat_scl = (size_t)f * d / 32;
   const long long total = words_exp * n_exp;
+  uint32_t smin = 255u, smax = 0u;  // range of the scale bytes this thread saw
   for (long long gw = blockIdx.x * (long long)blockDim.x + threadIdx.x; gw < total;
        gw += (long long)gridDim.x * blockDim.x) {
     const int e = (int)(gw / words_exp);
@@ -66,10 +67,20 @@ __global__ void pack_kernel(const uint8_t* __restrict__ canon_nib, const uint8_t
         const uint32_t sv = scl[(size_t)row * sb + kt * 4 + b];
         if (sv == 255u) atomicOr(bad, 1);  // E8M0 NaN: refused
         if (sv == 0u) atomicOr(bad, 2);    // 2^-127: kernels take the exact subnormal path
+        smin = min(smin, sv);
+        smax = max(smax, sv);
         word |= sv << (8 * b);
       }
     }
     reinterpret_cast<uint32_t*>(dst + (size_t)e * exp_bytes + (size_t)tile * kTileBytes)[wt] = word;
+  }
+  // bad[1], bad[2]: smallest and largest scale byte of the layer (the tensor-core path needs
+  // their span to fit fp16)
+  smin = __reduce_min_sync(0xffffffffu, smin);
+  smax = __reduce_max_sync(0xffffffffu, smax);
+  if ((threadIdx.x & 31) == 0) {
+    if (smin != 255u) atomicMin(bad + 1, (int32_t)smin);
+    if (smax != 0u) atomicMax(bad + 2, (int32_t)smax);
   }
 }
 
