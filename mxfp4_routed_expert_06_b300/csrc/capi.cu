@@ -84,6 +84,7 @@ struct k3moe_layer {
   uint8_t* packed = nullptr;    // device, E * exp_bytes (device mode)
   uint8_t* pool = nullptr;      // pinned host, E * exp_bytes (cache mode)
   float* Wr = nullptr;          // device [E][d]
+  uint16_t* Wsplit = nullptr;   // device [E][2d] bf16: W_r rounded (hi) then the rounding remainder (lo)
   float* bias = nullptr;        // device [E] or nullptr
   const uint8_t** eptr_dev = nullptr;  // device [E]
   const uint8_t** eptr_host = nullptr; // pinned host [E] (cache mode staging)
@@ -93,6 +94,7 @@ struct k3moe_layer {
   k3moe_cache* cache = nullptr;
   int uid = 0;
   int path = K3MOE_PATH_AUTO;
+  long long router_tc_min_t = 64;  // from this many tokens the logits run on the tensor cores
   long long gemm_min_t = 1LL << 40;
   bool profiling = false;
   std::vector<TimedLaunch> timed;
@@ -199,6 +201,7 @@ void free_layer(k3moe_layer* L) {
   cudaFree(L->packed);
   cudaFreeHost(L->pool);
   cudaFree(L->Wr);
+  cudaFree(L->Wsplit);
   cudaFree(L->bias);
   cudaFree((void*)L->eptr_dev);
   cudaFreeHost((void*)L->eptr_host);
@@ -232,13 +235,22 @@ bool use_gemm(const k3moe_layer* L, int T) {
   return (long long)T >= L->gemm_min_t && gemm_scales_ok(L->s_min, L->s_max);
 }
 
-// Router + selection + bucketing into the workspace.
-int run_routing(k3moe_layer* L, const void* x, int T, cudaStream_t s) {
+// Router + selection + bucketing into the workspace.  need_frag: the register-decode FFN
+// follows, which needs the fp16 fragments of x that the CUDA-core router kernel writes; without
+// it, many tokens take the tensor-core router (logits only).
+int run_routing(k3moe_layer* L, const void* x, int T, cudaStream_t s, bool need_frag) {
   const k3moe_dims& D = L->dims;
   RouterArgs ra{reinterpret_cast<const uint16_t*>(x), L->Wr, L->bias, T, D.d, D.E, D.k, L->ws, 0};
   // the last router block selects serially token by token: worth it only for a few tokens
   ra.fuse_select = (T <= 4 && T * D.k <= 1024) ? 1 : 0;
-  int rc = timed_launch(L, KID_ROUTER, s, [&] { return launch_router(ra, s); });
+  const bool tc = !need_frag && !ra.fuse_select && (long long)T >= L->router_tc_min_t &&
+                  (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
+  int rc = tc ? timed_launch(L, KID_ROUTER, s,
+                             [&] {
+                               return launch_router_tc(reinterpret_cast<const uint16_t*>(x), T, D.d, D.E, L->Wsplit,
+                                                       L->ws.logits, L->ws.sync + 1, L->wait_ns, L->num_sms, s);
+                             })
+              : timed_launch(L, KID_ROUTER, s, [&] { return launch_router(ra, s); });
   if (rc) return rc;
   if (!ra.fuse_select) {
     rc = timed_launch(L, KID_TOPK, s,
@@ -320,7 +332,7 @@ int make_resident(k3moe_layer* L, cudaStream_t s) {
 // Large T: the tcgen05 grouped GEMM path (gemm_tc.cu), then the slot-ordered combine.
 int forward_gemm(k3moe_layer* L, const void* x, int T, float* y, cudaStream_t s) {
   const k3moe_dims& D = L->dims;
-  int rc = run_routing(L, x, T, s);
+  int rc = run_routing(L, x, T, s, false);
   if (rc) return rc;
   if (L->cache) {
     rc = make_resident(L, s);
@@ -375,7 +387,7 @@ int forward_impl(k3moe_layer* L, const void* x, int T, float* y, cudaStream_t s)
                   L->s_min, L->s_max);
     return forward_gemm(L, x, T, y, s);
   }
-  int rc = run_routing(L, x, T, s);
+  int rc = run_routing(L, x, T, s, true);
   if (rc) return rc;
   if (L->cache) {
     rc = make_resident(L, s);
@@ -512,6 +524,12 @@ int k3moe_pack_experts(const k3moe_dims* dims, const void* canon_nib, const void
   if (to_device(L->Wr, W_r, (size_t)D.E * D.d * 4, src_on_device, s) != cudaSuccess ||
       (bias && to_device(L->bias, bias, (size_t)D.E * 4, src_on_device, s) != cudaSuccess))
     return bail(fail(K3MOE_ERR_CUDA, "router copy failed: %s", cudaGetErrorString(cudaGetLastError())));
+  if (cudaMalloc(&L->Wsplit, (size_t)D.E * D.d * 4) != cudaSuccess) {
+    cudaGetLastError();
+    return bail(fail(K3MOE_ERR_OOM, "router split weights allocation failed"));
+  }
+  if (launch_split_router(L->Wr, D.E, D.d, L->Wsplit, s) != cudaSuccess)
+    return bail(fail(K3MOE_ERR_CUDA, "router split failed: %s", cudaGetErrorString(cudaGetLastError())));
 
   const size_t cn = 3ull * D.f * D.d / 2, cs = 3ull * D.f * D.d / 32;
   // chunk of experts packed per pass: bounded staging (about 2 GB)
@@ -636,7 +654,7 @@ int k3moe_router_topk(k3moe_layer* L, const void* x, int T, int32_t* idx, float*
   if (T < 1 || T > L->dims.T_max) return fail(K3MOE_ERR_INVALID_ARG, "T=%d must be in 1..%d", T, L->dims.T_max);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   L->last_stream = s;
-  int rc = run_routing(L, x, T, s);
+  int rc = run_routing(L, x, T, s, false);
   if (rc) return rc;
   const size_t n = (size_t)T * L->dims.k;
   CUDA_TRY(cudaMemcpyAsync(idx, L->ws.idx, n * 4, cudaMemcpyDeviceToDevice, s));

@@ -36,6 +36,7 @@
 // with the 128-byte swizzle; 4 stages.  Two accumulators (2 x 256 TMEM columns) let the
 // epilogue of one item overlap the MMAs of the next.  Every wait is bounded (globaltimer).
 #include <cuda.h>
+#include <cuda_bf16.h>
 
 #include "k3moe_internal.cuh"
 
@@ -170,6 +171,8 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+// same with A and B bf16 (bits 7-9 and 10-12 = 1)
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) { return idesc_f16(M, N) | (1u << 7) | (1u << 10); }
 
 __device__ __forceinline__ void dec4(uint32_t w, uint32_t (&a)[4]) {
   asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t"
@@ -226,7 +229,9 @@ constexpr size_t kGemmSmem = 1024 + (size_t)kStages * kStageBytes + 256;
 struct GemmArgs {
   const uint8_t* const* expert_ptr;
   int d, f, k, T;
-  int mode;                 // 0: gate/up + SwiGLU, 1: down
+  int mode;                 // 0: gate/up + SwiGLU, 1: down, 2: router logits
+  int E;                    // router: experts (B rows)
+  float* logits;            // router output [T][E]
   int bn;                   // N of a work item: 256 (GU: 128 gate + 128 up rows; DN: 256 rows) or 128 (DN)
   int s_ref;
   float wscale;             // 2^(s_ref - 127)
@@ -254,9 +259,12 @@ struct Raw {
   uint2 s0, s1;
 };
 
-// tmap_a: 2-D map of the activation rows (fp16 [P][K], box 64 x 128, 128-byte swizzle)
+// tmap_a: 2-D map of the activation rows (fp16 [P][K], or bf16 x [T][d] for the router; box
+// 64 x 128, 128-byte swizzle).  tmap_b (router only): W_r split into bf16 hi and lo halves,
+// [E][2d], box 64 x 128.
 template <int MODE>
-__global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, GemmArgs a) {
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b, GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kStages * kStageBytes);
@@ -269,7 +277,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1 + kDecWarps);
+      mbar_init(&full[s], MODE == 2 ? 1 : 1 + kDecWarps);
       mbar_init(&empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -288,11 +296,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const int K = MODE == 0 ? a.d : a.f;
+  // router: K runs over [x | x] against [W_hi | W_lo], i.e. 2d values
+  const int K = MODE == 0 ? a.d : (MODE == 1 ? a.f : 2 * a.d);
   const int KS = K / kBK;
+  const int KSh = a.d / kBK;
   const int KT = K / kTileCols;
-  const int NT = MODE == 0 ? a.f / 128 : a.d / a.bn;
-  const int n_items = *a.nmtiles * NT;
+  const int NT = MODE == 0 ? a.f / 128 : (MODE == 1 ? a.d / a.bn : (a.E + 127) / 128);
+  const int n_items = (MODE == 2 ? (a.T + kBM - 1) / kBM : *a.nmtiles) * NT;
   const int G = gridDim.x;
   const uint32_t sbase = smem_u32(smem);
 
@@ -304,12 +314,40 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       if (!wait_phase(&accf[acc], (uint32_t)(use & 1), a.err, a.wait_ns)) break;
       tc_fence_after();
       const int mt = i / NT, nt = i % NT;
-      const int4 tile = __ldg(a.mtiles + mt);
       const int r = warp * 32 + lane;
+      const uint32_t tb = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(acc * 256);
+      if (MODE == 2) {
+        const int row = mt * kBM + r;
+        const bool valid = row < a.T;
+        const int c0 = nt * 128;
+        float* dst = a.logits + (size_t)(valid ? row : 0) * a.E + c0;
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tb + 32 * c, v);
+          tmem_ld_wait();
+          if (valid) {
+            if ((a.E & 3) == 0 && c0 + 32 * c + 32 <= a.E) {
+              float4* d4 = reinterpret_cast<float4*>(dst + 32 * c);
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                d4[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                    __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (c0 + 32 * c + j < a.E) dst[32 * c + j] = __uint_as_float(v[j]);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acce[acc]);
+        continue;
+      }
+      const int4 tile = __ldg(a.mtiles + mt);
       const bool valid = r < tile.z;
       const int pos = tile.y + (valid ? r : 0);
       const int p = __ldg(a.perm + pos);
-      const uint32_t tb = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(acc * 256);
       if (MODE == 0) {
         const float sc = __ldg(a.ascale + p / a.k) * a.wscale;
         float mx = 0.f;
@@ -358,7 +396,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   } else if (warp == kMmaWarp) {
     // ----------------------------------------------------------------- MMA issue ---
     if (lane == 0) {
-      const uint32_t idesc = idesc_f16(kBM, a.bn);
+      const uint32_t idesc = MODE == 2 ? idesc_bf16(kBM, 128) : idesc_f16(kBM, a.bn);
       uint32_t g = 0;
       int it = 0;
       bool ok = true;
@@ -392,18 +430,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     // ------------------------------------------------------------- A (TMA) issue ---
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
+      if (MODE == 2) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
       uint32_t g = 0;
       bool ok = true;
       for (int i = blockIdx.x; i < n_items && ok; i += G) {
-        const int row0 = __ldg(&a.mtiles[i / NT].y);
+        const int row0 = MODE == 2 ? (i / NT) * kBM : __ldg(&a.mtiles[i / NT].y);
         for (int ks = 0; ks < KS; ++ks, ++g) {
           const int slot = (int)(g % kStages);
           if (!wait_phase(&empty[slot], ((g / kStages) & 1u) ^ 1u, a.err, a.wait_ns)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[slot], (uint32_t)kABytes);
-          tma_load_2d(sbase + (uint32_t)(slot * kStageBytes), &tmap_a, ks * kBK, row0, &full[slot]);
+          const uint32_t st = sbase + (uint32_t)(slot * kStageBytes);
+          if (MODE == 2) {
+            mbar_arrive_expect_tx(&full[slot], (uint32_t)(kABytes + 128 * kBK * 2));
+            tma_load_2d(st, &tmap_a, (ks % KSh) * kBK, row0, &full[slot]);
+            tma_load_2d(st + kABytes, &tmap_b, ks * kBK, (i % NT) * 128, &full[slot]);
+          } else {
+            mbar_arrive_expect_tx(&full[slot], (uint32_t)kABytes);
+            tma_load_2d(st, &tmap_a, ks * kBK, row0, &full[slot]);
+          }
         }
       }
       // no load may be in flight when the CTA exits: the last use of each slot has completed
@@ -412,7 +458,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         wait_phase_drain(&full[q % kStages], (q / kStages) & 1u, a.err, a.wait_ns);
     }
     __syncwarp();
-  } else {
+  } else if (MODE != 2) {
     // ---------------------------------------------------------------- B decoders ---
     const int dw = warp - kDecWarp0;
     const int gq = lane >> 2, tq = lane & 3;
@@ -630,29 +676,31 @@ EncodeTiledFn encode_tiled() {
   return fn;
 }
 
-// fp16 [rows][K] row-major, boxes of 64 x 128 with the 128-byte swizzle the MMA descriptors use
-cudaError_t activation_map(CUtensorMap* m, const __half* base, int K, int rows) {
+// 16-bit [rows][K] row-major, boxes of 64 x 128 with the 128-byte swizzle the MMA descriptors use
+cudaError_t activation_map(CUtensorMap* m, const void* base, int K, int rows,
+                           CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_FLOAT16) {
   const EncodeTiledFn fn = encode_tiled();
   if (!fn) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
   const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBM};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(base), dims, strides, box, estr,
+  const CUresult r = fn(m, type, 2, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 template <int MODE>
-cudaError_t launch_gemm_mode(const CUtensorMap& map, const GemmArgs& g, int grid, cudaStream_t s) {
+cudaError_t launch_gemm_mode(const CUtensorMap& map, const CUtensorMap& map_b, const GemmArgs& g, int grid,
+                             cudaStream_t s) {
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  gemm_kernel<MODE><<<grid, kGemmThreads, kGemmSmem, s>>>(map, g);
+  gemm_kernel<MODE><<<grid, kGemmThreads, kGemmSmem, s>>>(map, map_b, g);
   return cudaGetLastError();
 }
 
@@ -702,7 +750,7 @@ cudaError_t launch_gemm_gu(const GemmFfn& q, cudaStream_t s) {
   CUtensorMap map;
   cudaError_t e = activation_map(&map, q.xg, q.d, q.T * q.k);
   if (e != cudaSuccess) return e;
-  return launch_gemm_mode<0>(map, g, q.num_sms, s);
+  return launch_gemm_mode<0>(map, map, g, q.num_sms, s);
 }
 
 cudaError_t launch_gemm_h16(const GemmFfn& q, int P, cudaStream_t s) {
@@ -718,7 +766,44 @@ cudaError_t launch_gemm_dn(const GemmFfn& q, cudaStream_t s) {
   CUtensorMap map;
   cudaError_t e = activation_map(&map, q.h16, q.f, q.T * q.k);
   if (e != cudaSuccess) return e;
-  return launch_gemm_mode<1>(map, g, q.num_sms, s);
+  return launch_gemm_mode<1>(map, map, g, q.num_sms, s);
+}
+
+cudaError_t launch_router_tc(const uint16_t* x, int T, int d, int E, const uint16_t* wsplit, float* logits,
+                             uint32_t* err, unsigned long long wait_ns, int num_sms, cudaStream_t s) {
+  GemmArgs g{};
+  g.d = d;
+  g.T = T;
+  g.E = E;
+  g.mode = 2;
+  g.bn = 128;
+  g.logits = logits;
+  g.err = err;
+  g.wait_ns = wait_ns;
+  CUtensorMap ma, mb;
+  cudaError_t e = activation_map(&ma, x, d, T, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+  if (e == cudaSuccess) e = activation_map(&mb, wsplit, 2 * d, E, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+  if (e != cudaSuccess) return e;
+  const int items = (T + kBM - 1) / kBM * ((E + 127) / 128);
+  return launch_gemm_mode<2>(ma, mb, g, items < num_sms ? items : num_sms, s);
+}
+
+// W_r fp32 [E][d] -> [E][2d] bf16: W_hi = bf16(W) then W_lo = bf16(W - W_hi)
+__global__ void split_router_kernel(const float* __restrict__ W, int E, int d, uint16_t* __restrict__ out) {
+  const size_t n = (size_t)E * d;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t e = i / d, j = i % d;
+    const float w = W[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(w - __bfloat162float(hi));
+    out[e * 2 * d + j] = __bfloat16_as_ushort(hi);
+    out[e * 2 * d + d + j] = __bfloat16_as_ushort(lo);
+  }
+}
+
+cudaError_t launch_split_router(const float* W, int E, int d, uint16_t* out, cudaStream_t s) {
+  split_router_kernel<<<1184, 256, 0, s>>>(W, E, d, out);
+  return cudaGetLastError();
 }
 
 }  // namespace k3

@@ -165,6 +165,11 @@ cudaError_t launch_gemm_prep(const GemmFfn& q, const uint16_t* x, const int32_t*
 cudaError_t launch_gemm_gu(const GemmFfn& q, cudaStream_t s);
 cudaError_t launch_gemm_h16(const GemmFfn& q, int P, cudaStream_t s);
 cudaError_t launch_gemm_dn(const GemmFfn& q, cudaStream_t s);
+// router logits on the tensor cores for large T: x (bf16 [T][d], 16-byte aligned) against W_r
+// split into bf16 hi and lo halves (wsplit [E][2d]) -> logits fp32 [T][E]
+cudaError_t launch_router_tc(const uint16_t* x, int T, int d, int E, const uint16_t* wsplit, float* logits,
+                             uint32_t* err, unsigned long long wait_ns, int num_sms, cudaStream_t s);
+cudaError_t launch_split_router(const float* W, int E, int d, uint16_t* out, cudaStream_t s);
 cudaError_t launch_residual_rmsnorm(const float* y, const uint16_t* x, int T, int d, float eps, uint16_t* x_next,
                                     uint16_t* x_norm, cudaStream_t s);
 

@@ -47,7 +47,10 @@ def test_noalloc_router_matches_layer_router(d, f, E, k, T, hot):
             k3.k3moe_router_topk_noalloc(x, Wr_d, bias_d, T, d, E, k, idx, w)
             torch.cuda.synchronize()
             assert torch.equal(idx, idx_ref), f"call {call}: expert ids differ"
-            np.testing.assert_allclose(w.cpu().numpy(), w_ref.cpu().numpy(), rtol=1e-5, atol=0)
+            # from 64 tokens the regular entry point computes the logits on the tensor cores
+            # (W_r split into bf16 hi + lo), so the weights agree to the bound the oracle
+            # comparisons use, not bitwise
+            np.testing.assert_allclose(w.cpu().numpy(), w_ref.cpu().numpy(), rtol=0, atol=1e-5)
     finally:
         k3.k3moe_layer_free(layer)
 
