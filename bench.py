@@ -231,14 +231,37 @@ def run_b300(args):
     weight_bytes_per_step = distinct * EXPERT_BYTES
 
     hbm_peak, bf16_peak, peak_kind = _peaks()
-    # dominant kernel: gate/up (two thirds of the streamed expert bytes)
-    gu_ms, gu_n = prof["gateup"]
-    gu_bytes_per_launch = (distinct / calls) * GATEUP_BYTES
-    achieved = gu_bytes_per_launch / (gu_ms / gu_n / 1e3) / 1e9 if gu_n else None
     launches = sum(v[1] for v in prof.values())
-    # the committed capture is of a T=1 launch; other workloads have no capture of their own
-    traffic = (_traffic_from_profile("mxfp4_routed_expert_06_b300/csrc/decode_ffn.cu", "gateup_decode_k3_t1.txt")
-               if T == 1 else None)
+    if prof["gemm_gu"][1]:
+        # tensor-core path: dominant kernel is the gate/up GEMM, 4*f*d flops per pick; fp16
+        # dense MMA runs at the bf16 rate, so the measured bf16 peak is the denominator
+        gu_ms, gu_n = prof["gemm_gu"]
+        flops = 4.0 * F * D * T * K
+        achieved = flops / (gu_ms / gu_n / 1e3) / 1e12
+        roofline = {"bound": "tensor", "kernel": "gemm_kernel<gate/up> (tcgen05, fp16 in, fp32 TMEM accumulate)",
+                    "achieved": round(achieved, 1), "peak": bf16_peak, "unit": "TFLOP/s",
+                    "frac": round(achieved / bf16_peak, 4),
+                    "peak_kind": f"{peak_kind} (cuBLAS bf16 dense, burst; fp16 dense has the same rate)",
+                    "algorithmic_flops_per_launch": flops,
+                    "traffic": _traffic_from_profile("mxfp4_routed_expert_06_b300/csrc/gemm_tc.cu",
+                                                     "gemm_gu_prefill_k3_t4096.txt") if T == 4096 else None}
+        dn_ms, dn_n = prof["gemm_dn"]
+        gemm_tflops = 6.0 * F * D * T * K / ((gu_ms / gu_n + dn_ms / dn_n) / 1e3) / 1e12
+    else:
+        # dominant kernel: gate/up (two thirds of the streamed expert bytes)
+        gu_ms, gu_n = prof["gateup"]
+        gu_bytes_per_launch = (distinct / calls) * GATEUP_BYTES
+        achieved = gu_bytes_per_launch / (gu_ms / gu_n / 1e3) / 1e9 if gu_n else None
+        # the committed capture is of a T=1 launch; other workloads have no capture of their own
+        traffic = (_traffic_from_profile("mxfp4_routed_expert_06_b300/csrc/decode_ffn.cu",
+                                         "gateup_decode_k3_t1.txt") if T == 1 else None)
+        roofline = {"bound": "hbm", "kernel": "gateup_kernel (gate/up + SwiGLU, register decode)",
+                    "achieved": None if achieved is None else round(achieved, 1),
+                    "peak": hbm_peak, "unit": "GB/s",
+                    "frac": None if achieved is None else round(achieved / hbm_peak, 4),
+                    "peak_kind": f"{peak_kind} (HBM copy peak)",
+                    "algorithmic_bytes_per_launch": int(gu_bytes_per_launch), "traffic": traffic}
+        gemm_tflops = None
 
     # end to end through the public host-buffer entry point
     xh = torch.from_numpy(xs.view(np.int16)).pin_memory()
@@ -273,16 +296,14 @@ def run_b300(args):
                                                  f" [profiling case: only {args.experts} experts resident]"),
                        "calls_per_step": calls, "tokens_per_step": tokens_per_step,
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                       "l2": "inputs larger than L2: 15.7 GB expert pool streamed from HBM; router L2-resident"},
+                       "l2": ("inputs larger than L2: 15.7 GB expert pool streamed from HBM; router L2-resident"
+                              if T < 4096 else "inputs larger than L2: 561 MB of hot experts, 1.9 GB of per-pick "
+                              "activations and outputs per call")},
             "weight_gbs": round(weight_bytes_per_step * args.steps * ws / (ms / 1e3) / 1e9, 1),
             "weight_pct_of_hbm_peak": round(100 * weight_bytes_per_step * args.steps / (ms / 1e3) / 1e9 / hbm_peak, 1),
             "distinct_experts_per_call": round(distinct / calls, 2),
-            "roofline": {"bound": "hbm", "kernel": "gateup_kernel (gate/up + SwiGLU, register decode)",
-                         "achieved": None if achieved is None else round(achieved, 1),
-                         "peak": hbm_peak, "unit": "GB/s",
-                         "frac": None if achieved is None else round(achieved / hbm_peak, 4),
-                         "peak_kind": f"{peak_kind} (HBM copy peak)",
-                         "algorithmic_bytes_per_launch": int(gu_bytes_per_launch), "traffic": traffic},
+            "roofline": roofline,
+            "expert_gemm_tflops": None if gemm_tflops is None else round(gemm_tflops, 1),
             "kernel_ms_per_launch": {k: round(v[0] / v[1], 5) for k, v in prof.items() if v[1]},
             "gpu_launches": int(launches),
             "e2e": {"value": round(e2e_val, 3), "unit": "tokens/s",

@@ -172,7 +172,9 @@ int k3moe_sync(k3moe_layer* layer);
 
 /* Options. */
 #define K3MOE_OPT_PATH 1        /* value: K3MOE_PATH_AUTO (default), _DECODE, _GEMM */
-#define K3MOE_OPT_GEMM_MIN_T 2  /* value: smallest T the AUTO path sends to the grouped GEMM */
+#define K3MOE_OPT_GEMM_MIN_T 2  /* value: smallest T the AUTO path sends to the grouped GEMM
+                                   (default 512; layers whose scale bytes span more than 36
+                                   steps always take the register-decode path under AUTO) */
 #define K3MOE_OPT_DEVICE_WAIT_NS 3  /* value: bound in ns on every device-side wait (1e6..6e10) */
 #define K3MOE_OPT_TEST_STALL 4  /* value 1: the next forward's FFN kernels wait on a barrier that
                                    nothing completes until the bound expires (failure-path test) */

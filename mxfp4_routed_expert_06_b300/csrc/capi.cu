@@ -95,7 +95,7 @@ struct k3moe_layer {
   int uid = 0;
   int path = K3MOE_PATH_AUTO;
   long long router_tc_min_t = 64;  // from this many tokens the logits run on the tensor cores
-  long long gemm_min_t = 1LL << 40;
+  long long gemm_min_t = 512;  // AUTO: from this many tokens the tensor-core GEMM path
   bool profiling = false;
   std::vector<TimedLaunch> timed;
   std::vector<cudaEvent_t> spare_events;
