@@ -231,6 +231,7 @@ __device__ __forceinline__ int warp_kts(int KT, int w) { return w < KT ? (KT - w
 
 template <int DEPTH, bool ZS>
 __global__ void __launch_bounds__(kGuThreads, 2) gateup_kernel(FfnArgs a, GuLayout L) {
+  pdl_entry();
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* red_full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* red_empty = red_full + kGuRed;
@@ -513,6 +514,7 @@ inline DnLayout dn_layout(int f, int mcap, size_t budget) {
 
 template <int DEPTH, bool ZS>
 __global__ void __launch_bounds__(kDnThreads, 2) down_kernel(FfnArgs a, DnLayout L) {
+  pdl_entry();
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -656,6 +658,7 @@ __global__ void __launch_bounds__(kDnThreads, 2) down_kernel(FfnArgs a, DnLayout
 // ------------------------------------------------------------------------- combine ---
 __global__ void __launch_bounds__(64) combine_kernel(const float* __restrict__ obuf, int T, int d, int k,
                                                       float* __restrict__ y) {
+  pdl_entry();
   const size_t n4 = (size_t)T * d / 4;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
     const size_t t = i / (d / 4), c4 = i % (d / 4);
@@ -701,8 +704,7 @@ cudaError_t launch_gu(const FfnArgs& a, const GuLayout& L, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  gateup_kernel<DEPTH, ZS><<<a.num_sms * kCtasPerSm, kGuThreads, L.total, s>>>(a, L);
-  return cudaGetLastError();
+  return launch_pdl(gateup_kernel<DEPTH, ZS>, dim3(a.num_sms * kCtasPerSm), dim3(kGuThreads), L.total, s, a, L);
 }
 
 template <int DEPTH, bool ZS>
@@ -714,8 +716,7 @@ cudaError_t launch_dn(const FfnArgs& a, const DnLayout& L, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  down_kernel<DEPTH, ZS><<<a.num_sms * kCtasPerSm, kDnThreads, L.total, s>>>(a, L);
-  return cudaGetLastError();
+  return launch_pdl(down_kernel<DEPTH, ZS>, dim3(a.num_sms * kCtasPerSm), dim3(kDnThreads), L.total, s, a, L);
 }
 
 }  // namespace
@@ -751,8 +752,7 @@ cudaError_t launch_down(const FfnArgs& a, cudaStream_t s) {
 cudaError_t launch_combine(const FfnArgs& a, cudaStream_t s) {
   const size_t n4 = (size_t)a.T * a.d / 4;
   const int grid = (int)std::min<size_t>((n4 + 63) / 64, (size_t)a.num_sms * 32);
-  combine_kernel<<<grid, 64, 0, s>>>(a.ws.obuf, a.T, a.d, a.k, a.y);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3(grid), dim3(64), 0, s, (const float*)a.ws.obuf, a.T, a.d, a.k, a.y);
 }
 
 }  // namespace k3

@@ -247,11 +247,6 @@ struct GemmArgs {
   unsigned long long wait_ns;
 };
 
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {
-  // byte offset of 16-byte chunk `chunk` (0..7) of row `row` in a K-major 128B-swizzled tile
-  return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4));
-}
-
 // Raw bytes one decoder lane needs for one stage: two tile halves (16 nibble bytes each) and
 // their scale words (rows g and g+8 x 4 blocks).
 struct Raw {
@@ -295,6 +290,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_entry();  // set-up above touched only shared and tensor memory
 
   // router: K runs over [x | x] against [W_hi | W_lo], i.e. 2d values
   const int K = MODE == 0 ? a.d : (MODE == 1 ? a.f : 2 * a.d);
@@ -576,6 +572,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 // per-token power of two: xs[t] = 2^q with max|x_t| * 2^-q in [2^14, 2^15)
 __global__ void __launch_bounds__(256) gemm_prep_x_kernel(const uint16_t* __restrict__ x, int d, float* xs) {
+  pdl_entry();
   __shared__ float part[8];
   const size_t base = (size_t)blockIdx.x * d;
   float mx = 0.f;
@@ -594,6 +591,7 @@ __global__ void __launch_bounds__(256) gemm_prep_x_kernel(const uint16_t* __rest
 __global__ void __launch_bounds__(128) gemm_gather_kernel(const uint16_t* __restrict__ x, const float* __restrict__ xs,
                                                           const int32_t* __restrict__ perm, int d, int k,
                                                           __half* __restrict__ xg) {
+  pdl_entry();
   const int t = __ldg(perm + blockIdx.x) / k;
   const float inv = 1.0f / __ldg(xs + t);  // a power of two: exact
   const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
@@ -615,6 +613,7 @@ __global__ void __launch_bounds__(128) gemm_gather_kernel(const uint16_t* __rest
 __global__ void __launch_bounds__(1024) gemm_tiles_kernel(const int32_t* __restrict__ counts,
                                                           const int32_t* __restrict__ offsets, int E, int4* mtiles,
                                                           int32_t* nmtiles) {
+  pdl_entry();
   __shared__ int wsum[32];
   const int per = (E + 1023) / 1024;
   const int e0 = threadIdx.x * per;
@@ -650,6 +649,7 @@ __global__ void __launch_bounds__(1024) gemm_tiles_kernel(const int32_t* __restr
 __global__ void __launch_bounds__(256) gemm_h16_kernel(const float* __restrict__ hbuf,
                                                        const uint32_t* __restrict__ hmax, int f, __half* h16,
                                                        float* hs) {
+  pdl_entry();
   const size_t base = (size_t)blockIdx.x * f;
   const int q = fp16_scale_exp(__uint_as_float(hmax[blockIdx.x]));
   const float inv = exp2i(-q);
@@ -700,8 +700,7 @@ cudaError_t launch_gemm_mode(const CUtensorMap& map, const CUtensorMap& map_b, c
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  gemm_kernel<MODE><<<grid, kGemmThreads, kGemmSmem, s>>>(map, map_b, g);
-  return cudaGetLastError();
+  return launch_pdl(gemm_kernel<MODE>, dim3(grid), dim3(kGemmThreads), kGemmSmem, s, map, map_b, g);
 }
 
 }  // namespace
@@ -710,14 +709,13 @@ bool gemm_scales_ok(int s_min, int s_max) { return s_max >= s_min && s_max - s_m
 
 cudaError_t launch_gemm_prep(const GemmFfn& q, const uint16_t* x, const int32_t* counts, const int32_t* offsets,
                              int E, cudaStream_t s) {
-  gemm_prep_x_kernel<<<q.T, 256, 0, s>>>(x, q.d, q.xs);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(gemm_prep_x_kernel, dim3(q.T), dim3(256), 0, s, x, q.d, q.xs);
   if (e != cudaSuccess) return e;
-  gemm_tiles_kernel<<<1, 1024, 0, s>>>(counts, offsets, E, const_cast<int4*>(q.mtiles), const_cast<int32_t*>(q.nmtiles));
-  e = cudaGetLastError();
+  e = launch_pdl(gemm_tiles_kernel, dim3(1), dim3(1024), 0, s, counts, offsets, E, const_cast<int4*>(q.mtiles),
+                 const_cast<int32_t*>(q.nmtiles));
   if (e != cudaSuccess) return e;
-  gemm_gather_kernel<<<q.T * q.k, 128, 0, s>>>(x, q.xs, q.perm, q.d, q.k, q.xg);
-  return cudaGetLastError();
+  return launch_pdl(gemm_gather_kernel, dim3(q.T * q.k), dim3(128), 0, s, x, (const float*)q.xs, (const int32_t*)q.perm,
+                    q.d, q.k, q.xg);
 }
 
 namespace {
@@ -754,8 +752,8 @@ cudaError_t launch_gemm_gu(const GemmFfn& q, cudaStream_t s) {
 }
 
 cudaError_t launch_gemm_h16(const GemmFfn& q, int P, cudaStream_t s) {
-  gemm_h16_kernel<<<P, 256, 0, s>>>(q.hbuf, q.hmax, q.f, q.h16, q.hs);
-  return cudaGetLastError();
+  return launch_pdl(gemm_h16_kernel, dim3(P), dim3(256), 0, s, (const float*)q.hbuf, (const uint32_t*)q.hmax, q.f,
+                    q.h16, q.hs);
 }
 
 cudaError_t launch_gemm_dn(const GemmFfn& q, cudaStream_t s) {

@@ -27,6 +27,7 @@ __global__ void __launch_bounds__(kGlueThreads) residual_rmsnorm_kernel(const fl
                                                                         const uint16_t* x, int d, float eps,
                                                                         uint16_t* x_next, uint16_t* x_norm) {
   __shared__ float part[kGlueThreads / 32];
+  pdl_entry();
   const size_t base = (size_t)blockIdx.x * d;
   float ss = 0.f;
   // each thread owns the elements j = tid + i*blockDim; it reads back only its own writes
@@ -50,8 +51,7 @@ __global__ void __launch_bounds__(kGlueThreads) residual_rmsnorm_kernel(const fl
 
 cudaError_t launch_residual_rmsnorm(const float* y, const uint16_t* x, int T, int d, float eps, uint16_t* x_next,
                                     uint16_t* x_norm, cudaStream_t s) {
-  residual_rmsnorm_kernel<<<T, kGlueThreads, 0, s>>>(y, x, d, eps, x_next, x_norm);
-  return cudaGetLastError();
+  return launch_pdl(residual_rmsnorm_kernel, dim3(T), dim3(kGlueThreads), 0, s, y, x, d, eps, x_next, x_norm);
 }
 
 }  // namespace k3

@@ -120,6 +120,32 @@ cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* coun
                           int32_t* perm, int32_t* act, int32_t* nact, UnitDesc* units, int32_t* nunits,
                           const float* w, const float* xscale, cudaStream_t s);
 
+// Programmatic dependent launch.  Every kernel of the forward path begins with pdl_entry(): it
+// waits until the previous kernel in the stream has completed and its writes are visible, then
+// lets the next kernel be scheduled.  Only launch latency and CTA start-up overlap; no kernel
+// touches global memory before its predecessor has finished.
+__device__ __forceinline__ void pdl_entry() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+  return e == cudaSuccess ? cudaGetLastError() : e;
+}
+
 // Device error flags (ws.sync[1]).
 constexpr uint32_t kErrTimeout = 1u;
 constexpr uint32_t kErrBadAccess = 2u;  // self-checking builds only: a copy address failed its check

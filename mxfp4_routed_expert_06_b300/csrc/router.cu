@@ -456,6 +456,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(RouterArgs a)
   __shared__ float red[kRouterWarps];
   __shared__ float half_sum[kRouterWarps * kTokTile];
   __shared__ int last;
+  pdl_entry();
   logits_and_convert(a, reinterpret_cast<uint16_t*>(rsm), red, half_sum);
   if (!a.fuse_select) return;
   __threadfence();
@@ -483,6 +484,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(RouterArgs a)
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* logits, const float* bias, int T, int E, int k,
                                                             int32_t* idx, float* w) {
   extern __shared__ __align__(16) uint8_t tsm[];
+  pdl_entry();
   uint32_t* ku = reinterpret_cast<uint32_t*>(tsm);
   float* sg = reinterpret_cast<float*>(ku + E);
   uint2* cand = reinterpret_cast<uint2*>(sg + E);  // word offset 2E: 8-byte aligned
@@ -495,6 +497,7 @@ __global__ void __launch_bounds__(1024) bucket_kernel(const int32_t* idx, int P,
                                                       UnitDesc* units, int32_t* nunits, const float* w,
                                                       const float* xscale) {
   extern __shared__ int ism[];
+  pdl_entry();
   bucket_block(idx, P, k, E, counts, offsets, perm, act, nact, units, nunits, w, xscale, ism, false);
 }
 
@@ -511,8 +514,7 @@ cudaError_t launch_router(const RouterArgs& a, cudaStream_t s) {
     attr = true;
   }
   const int grid = (a.E + kRowsPerCta - 1) / kRowsPerCta;
-  router_kernel<<<grid, kRouterWarps * 32, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(router_kernel, dim3(grid), dim3(kRouterWarps * 32), smem, s, a);
 }
 
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* idx, float* w,
@@ -523,8 +525,7 @@ cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, in
     attr = true;
   }
   const size_t smem = (size_t)(2 * E + 2) * 4 + 256 * 8;
-  topk_kernel<<<std::min(T, 148 * 8), kTopkThreads, smem, s>>>(logits, bias, T, E, k, idx, w);
-  return cudaGetLastError();
+  return launch_pdl(topk_kernel, dim3(std::min(T, 148 * 8)), dim3(kTopkThreads), smem, s, logits, bias, T, E, k, idx, w);
 }
 
 cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* counts, int32_t* offsets,
@@ -535,9 +536,8 @@ cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* coun
     cudaFuncSetAttribute(bucket_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
     attr = true;
   }
-  bucket_kernel<<<1, 1024, (size_t)2 * E * sizeof(int), s>>>(idx, T * k, k, E, counts, offsets, perm, act, nact,
-                                                              units, nunits, w, xscale);
-  return cudaGetLastError();
+  return launch_pdl(bucket_kernel, dim3(1), dim3(1024), (size_t)2 * E * sizeof(int), s, idx, T * k, k, E, counts,
+                    offsets, perm, act, nact, units, nunits, w, xscale);
 }
 
 }  // namespace k3
