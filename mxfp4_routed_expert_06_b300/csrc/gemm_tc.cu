@@ -25,16 +25,19 @@
 //   gemm_kernel<DN>      [picks of e] x [down rows of e]^T, times the combine weight,
 //                        -> obuf[pick][d]; the combine kernel then sums the k slots in order.
 //
-// gemm_kernel is persistent (one CTA per SM, work item = (M-tile, N-tile)), with warp roles:
+// gemm_kernel is persistent (one CTA per SM).  A work item is (two consecutive 128-row M-tiles
+// of one expert, N tile): every decoded weight stage feeds the MMAs of both M-tiles, which
+// halves the decode work per flop.  Warp roles:
 //   warps 0-3   epilogue: TMEM -> registers (warp w reads TMEM lanes 32w..32w+31 = tile rows)
-//   warp  4     TMEM allocation; lane 0 issues the MMAs (M=128, N=256 or 128, K=16 each)
-//   warp  5     lane 0 issues one 2-D TMA load per stage of the tile's 128 activation rows
+//   warp  4     TMEM allocation; lane 0 issues the MMAs (M=128, N=256 or 128, K=16 each; the two
+//               M-tiles accumulate in TMEM columns 0.. and 256..)
+//   warp  5     lane 0 issues the 2-D TMA loads of the item's activation rows per stage
 //               (rows are contiguous: xg for GU, h16 for DN, both in bucketed order)
 //   warps 6-13  B decoders: MXFP4 bytes (registers, prefetched 4 stages ahead) ->
 //               cvt e2m1x2 -> f16x2, times 2^(s-s_ref) -> shared memory
-// A stage is 64 values of K: A 128x64 fp16 (16 KB) + B up to 256x64 fp16 (32 KB), both K-major
-// with the 128-byte swizzle; 4 stages.  Two accumulators (2 x 256 TMEM columns) let the
-// epilogue of one item overlap the MMAs of the next.  Every wait is bounded (globaltimer).
+// A stage is 64 values of K: A 2 x 128x64 fp16 (2 x 16 KB) + B up to 256x64 fp16 (32 KB), all
+// K-major with the 128-byte swizzle; 3 stages.  The epilogue drains both accumulators before
+// the next item's MMAs start.  Every wait is bounded (globaltimer).
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -209,19 +212,19 @@ __device__ __forceinline__ int fp16_scale_exp(float m) {
 __device__ __forceinline__ float exp2i(int q) { return __uint_as_float((uint32_t)(127 + q) << 23); }
 
 // ----------------------------------------------------------------------- constants ---
-constexpr int kStages = 4;
-constexpr int kBM = 128;                 // rows (picks) per M-tile
+constexpr int kStages = 3;
+constexpr int kBM = 128;                 // rows (picks) per M-tile; a work item has two
 constexpr int kBK = 64;                  // K values per stage
-constexpr int kABytes = kBM * kBK * 2;   // 16 KB
+constexpr int kABytes = kBM * kBK * 2;   // 16 KB per M-tile
 constexpr int kBBytes = 256 * kBK * 2;   // 32 KB (N up to 256)
-constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kStageBytes = 2 * kABytes + kBBytes;  // A of both M-tiles, then B
 constexpr int kEpiWarps = 4;
 constexpr int kMmaWarp = 4;
 constexpr int kTmaWarp = 5;
 constexpr int kDecWarp0 = 6;
 constexpr int kDecWarps = 8;
 constexpr int kGemmThreads = (kDecWarp0 + kDecWarps) * 32;  // 448
-constexpr int kTmemCols = 512;           // two accumulators of up to 256 fp32 columns
+constexpr int kTmemCols = 512;           // accumulators of the two M-tiles, up to 256 fp32 columns each
 constexpr int kPf = 4;                   // B decoders: stages of raw bytes held in registers
 // shared memory: stages, then barriers; +1024 for alignment
 constexpr size_t kGemmSmem = 1024 + (size_t)kStages * kStageBytes + 256;
@@ -235,7 +238,7 @@ struct GemmArgs {
   int bn;                   // N of a work item: 256 (GU: 128 gate + 128 up rows; DN: 256 rows) or 128 (DN)
   int s_ref;
   float wscale;             // 2^(s_ref - 127)
-  const int4* mtiles;       // {expert, first bucketed row, rows, 0}
+  const int4* mtiles;       // {expert, first bucketed row, rows of M-tile 0, rows of M-tile 1}
   const int32_t* nmtiles;
   const int32_t* perm;      // bucketed row -> pick id
   const float* wgt;         // [P] combine weights by pick
@@ -254,6 +257,21 @@ struct Raw {
   uint2 s0, s1;
 };
 
+// Work item i = (pair of M-tiles i / NT, N tile i % NT).  The pair: two consecutive 128-row
+// M-tiles of one expert (the second may be empty); for the router, 256 consecutive tokens.
+struct Pair {
+  int e, row0, rows0, rows1;
+};
+template <int MODE>
+__device__ __forceinline__ Pair pair_of(const GemmArgs& a, int pt) {
+  if (MODE == 2) {
+    const int row0 = pt * 2 * kBM;
+    return Pair{0, row0, min(kBM, a.T - row0), max(0, min(kBM, a.T - row0 - kBM))};
+  }
+  const int4 v = __ldg(a.mtiles + pt);
+  return Pair{v.x, v.y, v.z, v.w};
+}
+
 // tmap_a: 2-D map of the activation rows (fp16 [P][K], or bf16 x [T][d] for the router; box
 // 64 x 128, 128-byte swizzle).  tmap_b (router only): W_r split into bf16 hi and lo halves,
 // [E][2d], box 64 x 128.
@@ -264,9 +282,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kStages * kStageBytes);
   uint64_t* empty = full + kStages;
-  uint64_t* accf = empty + kStages;  // [2] accumulator ready
-  uint64_t* acce = accf + 2;         // [2] accumulator drained by the epilogue
-  uint64_t* drain = acce + 2;        // final MMA completion
+  uint64_t* accf = empty + kStages;  // accumulators ready
+  uint64_t* acce = accf + 1;         // accumulators drained by the epilogue
+  uint64_t* drain = acce + 1;        // final MMA completion
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -275,10 +293,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&full[s], MODE == 2 ? 1 : 1 + kDecWarps);
       mbar_init(&empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&accf[i], 1);
-      mbar_init(&acce[i], kEpiWarps);
-    }
+    mbar_init(accf, 1);
+    mbar_init(acce, kEpiWarps);
     mbar_init(drain, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -298,7 +314,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int KSh = a.d / kBK;
   const int KT = K / kTileCols;
   const int NT = MODE == 0 ? a.f / 128 : (MODE == 1 ? a.d / a.bn : (a.E + 127) / 128);
-  const int n_items = (MODE == 2 ? (a.T + kBM - 1) / kBM : *a.nmtiles) * NT;
+  const int n_items = (MODE == 2 ? (a.T + 2 * kBM - 1) / (2 * kBM) : *a.nmtiles) * NT;
   const int G = gridDim.x;
   const uint32_t sbase = smem_u32(smem);
 
@@ -306,88 +322,86 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ------------------------------------------------------------------ epilogue ---
     int it = 0;
     for (int i = blockIdx.x; i < n_items; i += G, ++it) {
-      const int acc = it & 1, use = it >> 1;
-      if (!wait_phase(&accf[acc], (uint32_t)(use & 1), a.err, a.wait_ns)) break;
+      if (!wait_phase(accf, (uint32_t)(it & 1), a.err, a.wait_ns)) break;
       tc_fence_after();
-      const int mt = i / NT, nt = i % NT;
+      const int nt = i % NT;
+      const Pair pr = pair_of<MODE>(a, i / NT);
       const int r = warp * 32 + lane;
-      const uint32_t tb = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(acc * 256);
-      if (MODE == 2) {
-        const int row = mt * kBM + r;
-        const bool valid = row < a.T;
-        const int c0 = nt * 128;
-        float* dst = a.logits + (size_t)(valid ? row : 0) * a.E + c0;
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tb + 32 * c, v);
-          tmem_ld_wait();
-          if (valid) {
-            if ((a.E & 3) == 0 && c0 + 32 * c + 32 <= a.E) {
+      for (int h = 0; h < 2; ++h) {
+        const int rows = h ? pr.rows1 : pr.rows0;
+        if (rows <= 0) continue;  // uniform across the warp
+        const uint32_t tb = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(h * 256);
+        const bool valid = r < rows;
+        const int pos = pr.row0 + h * kBM + (valid ? r : 0);
+        if (MODE == 2) {
+          const int c0 = nt * 128;
+          float* dst = a.logits + (size_t)pos * a.E + c0;
+          for (int c = 0; c < 4; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tb + 32 * c, v);
+            tmem_ld_wait();
+            if (valid) {
+              if ((a.E & 3) == 0 && c0 + 32 * c + 32 <= a.E) {
+                float4* d4 = reinterpret_cast<float4*>(dst + 32 * c);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                  d4[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                      __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (c0 + 32 * c + j < a.E) dst[32 * c + j] = __uint_as_float(v[j]);
+              }
+            }
+          }
+          continue;
+        }
+        const int p = __ldg(a.perm + pos);
+        if (MODE == 0) {
+          const float sc = __ldg(a.ascale + p / a.k) * a.wscale;
+          float mx = 0.f;
+          float* dst = a.hbuf + (size_t)pos * a.f + nt * 128;
+          for (int c = 0; c < 4; ++c) {
+            uint32_t gr[32], ur[32];
+            tmem_ld32(tb + 32 * c, gr);
+            tmem_ld32(tb + 128 + 32 * c, ur);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float g = __uint_as_float(gr[j]) * sc, u = __uint_as_float(ur[j]) * sc;
+              const float hv = g / (1.0f + expf(-g)) * u;
+              gr[j] = __float_as_uint(hv);
+              mx = fmaxf(mx, fabsf(hv));
+            }
+            if (valid) {
               float4* d4 = reinterpret_cast<float4*>(dst + 32 * c);
 #pragma unroll
               for (int q = 0; q < 8; ++q)
-                d4[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                    __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (c0 + 32 * c + j < a.E) dst[32 * c + j] = __uint_as_float(v[j]);
+                d4[q] = make_float4(__uint_as_float(gr[4 * q]), __uint_as_float(gr[4 * q + 1]),
+                                    __uint_as_float(gr[4 * q + 2]), __uint_as_float(gr[4 * q + 3]));
             }
           }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acce[acc]);
-        continue;
-      }
-      const int4 tile = __ldg(a.mtiles + mt);
-      const bool valid = r < tile.z;
-      const int pos = tile.y + (valid ? r : 0);
-      const int p = __ldg(a.perm + pos);
-      if (MODE == 0) {
-        const float sc = __ldg(a.ascale + p / a.k) * a.wscale;
-        float mx = 0.f;
-        float* dst = a.hbuf + (size_t)pos * a.f + nt * 128;
-        for (int c = 0; c < 4; ++c) {
-          uint32_t gr[32], ur[32];
-          tmem_ld32(tb + 32 * c, gr);
-          tmem_ld32(tb + 128 + 32 * c, ur);
-          tmem_ld_wait();
+          if (valid) atomicMax(a.hmax + pos, __float_as_uint(mx));
+        } else {
+          const float sc = __ldg(a.ascale + pos) * a.wscale * __ldg(a.wgt + p);
+          float* dst = a.obuf + (size_t)p * a.d + (size_t)nt * a.bn;
+          for (int c = 0; c < a.bn / 32; ++c) {
+            uint32_t orr[32];
+            tmem_ld32(tb + 32 * c, orr);
+            tmem_ld_wait();
+            if (valid) {
+              float4* d4 = reinterpret_cast<float4*>(dst + 32 * c);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float g = __uint_as_float(gr[j]) * sc, u = __uint_as_float(ur[j]) * sc;
-            const float h = g / (1.0f + expf(-g)) * u;
-            gr[j] = __float_as_uint(h);
-            mx = fmaxf(mx, fabsf(h));
-          }
-          if (valid) {
-            float4* d4 = reinterpret_cast<float4*>(dst + 32 * c);
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              d4[q] = make_float4(__uint_as_float(gr[4 * q]), __uint_as_float(gr[4 * q + 1]),
-                                  __uint_as_float(gr[4 * q + 2]), __uint_as_float(gr[4 * q + 3]));
-          }
-        }
-        if (valid) atomicMax(a.hmax + pos, __float_as_uint(mx));
-      } else {
-        const float sc = __ldg(a.ascale + pos) * a.wscale * __ldg(a.wgt + p);
-        float* dst = a.obuf + (size_t)p * a.d + (size_t)nt * a.bn;
-        for (int c = 0; c < a.bn / 32; ++c) {
-          uint32_t orr[32];
-          tmem_ld32(tb + 32 * c, orr);
-          tmem_ld_wait();
-          if (valid) {
-            float4* d4 = reinterpret_cast<float4*>(dst + 32 * c);
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              d4[q] = make_float4(__uint_as_float(orr[4 * q]) * sc, __uint_as_float(orr[4 * q + 1]) * sc,
-                                  __uint_as_float(orr[4 * q + 2]) * sc, __uint_as_float(orr[4 * q + 3]) * sc);
+              for (int q = 0; q < 8; ++q)
+                d4[q] = make_float4(__uint_as_float(orr[4 * q]) * sc, __uint_as_float(orr[4 * q + 1]) * sc,
+                                    __uint_as_float(orr[4 * q + 2]) * sc, __uint_as_float(orr[4 * q + 3]) * sc);
+            }
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acce[acc]);
+      if (lane == 0) mbar_arrive(acce);
     }
   } else if (warp == kMmaWarp) {
     // ----------------------------------------------------------------- MMA issue ---
@@ -397,10 +411,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int it = 0;
       bool ok = true;
       for (int i = blockIdx.x; i < n_items && ok; i += G, ++it) {
-        const int acc = it & 1, use = it >> 1;
-        if (!wait_phase(&acce[acc], (uint32_t)((use & 1) ^ 1), a.err, a.wait_ns)) break;
+        const bool two = pair_of<MODE>(a, i / NT).rows1 > 0;
+        if (!wait_phase(acce, (uint32_t)((it & 1) ^ 1), a.err, a.wait_ns)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem + (uint32_t)(acc * 256);
         for (int ks = 0; ks < KS; ++ks, ++g) {
           const int slot = (int)(g % kStages);
           if (!wait_phase(&full[slot], (g / kStages) & 1u, a.err, a.wait_ns)) {
@@ -409,13 +422,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           tc_fence_after();
           const uint32_t as = sbase + (uint32_t)(slot * kStageBytes);
-          const uint64_t ad = smem_desc(as), bd = smem_desc(as + kABytes);
+          const uint64_t a0 = smem_desc(as), a1 = smem_desc(as + kABytes), bd = smem_desc(as + 2 * kABytes);
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)  // +32 bytes along K per k16 step
-            mma_f16(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, (ks | kk) != 0 ? 1u : 0u);
+          for (int kk = 0; kk < kBK / 16; ++kk) {  // +32 bytes along K per k16 step
+            const uint32_t accum = (ks | kk) != 0 ? 1u : 0u;
+            mma_f16(tmem, a0 + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, accum);
+            if (two) mma_f16(tmem + 256u, a1 + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, accum);
+          }
           mma_commit(&empty[slot]);
         }
-        if (ok) mma_commit(&accf[acc]);
+        if (ok) mma_commit(accf);
       }
       // everything issued has completed before TMEM is released
       mma_commit(drain);
@@ -430,7 +446,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t g = 0;
       bool ok = true;
       for (int i = blockIdx.x; i < n_items && ok; i += G) {
-        const int row0 = MODE == 2 ? (i / NT) * kBM : __ldg(&a.mtiles[i / NT].y);
+        const Pair pr = pair_of<MODE>(a, i / NT);
+        const bool two = pr.rows1 > 0;
         for (int ks = 0; ks < KS; ++ks, ++g) {
           const int slot = (int)(g % kStages);
           if (!wait_phase(&empty[slot], ((g / kStages) & 1u) ^ 1u, a.err, a.wait_ns)) {
@@ -438,14 +455,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           const uint32_t st = sbase + (uint32_t)(slot * kStageBytes);
-          if (MODE == 2) {
-            mbar_arrive_expect_tx(&full[slot], (uint32_t)(kABytes + 128 * kBK * 2));
-            tma_load_2d(st, &tmap_a, (ks % KSh) * kBK, row0, &full[slot]);
-            tma_load_2d(st + kABytes, &tmap_b, ks * kBK, (i % NT) * 128, &full[slot]);
-          } else {
-            mbar_arrive_expect_tx(&full[slot], (uint32_t)kABytes);
-            tma_load_2d(st, &tmap_a, ks * kBK, row0, &full[slot]);
-          }
+          const int kc = MODE == 2 ? (ks % KSh) * kBK : ks * kBK;
+          const uint32_t bytes = (uint32_t)kABytes * (two ? 2u : 1u) + (MODE == 2 ? 128u * kBK * 2u : 0u);
+          mbar_arrive_expect_tx(&full[slot], bytes);
+          tma_load_2d(st, &tmap_a, kc, pr.row0, &full[slot]);
+          if (two) tma_load_2d(st + kABytes, &tmap_a, kc, pr.row0 + kBM, &full[slot]);
+          if (MODE == 2) tma_load_2d(st + 2 * kABytes, &tmap_b, ks * kBK, (i % NT) * 128, &full[slot]);
         }
       }
       // no load may be in flight when the CTA exits: the last use of each slot has completed
@@ -544,7 +559,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             ok = false;
           } else {
             const int u = (s % KS) & 1;
-            const uint32_t bs = sbase + (uint32_t)(slot * kStageBytes + kABytes);
+            const uint32_t bs = sbase + (uint32_t)(slot * kStageBytes + 2 * kABytes);
             if (MODE == 0) {
               decode(raw[j].n0, raw[j].s0, u, 16 * dw, bs);        // gate rows
               decode(raw[j].n1, raw[j].s1, u, 128 + 16 * dw, bs);  // up rows
@@ -609,7 +624,8 @@ __global__ void __launch_bounds__(128) gemm_gather_kernel(const uint16_t* __rest
   }
 }
 
-// M-tiles: for each expert e (ascending) ceil(count/128) tiles of consecutive bucketed rows
+// M-tile pairs: for each expert e (ascending) ceil(count/256) pairs of 128-row tiles of
+// consecutive bucketed rows (the second tile of the last pair may be short or empty)
 __global__ void __launch_bounds__(1024) gemm_tiles_kernel(const int32_t* __restrict__ counts,
                                                           const int32_t* __restrict__ offsets, int E, int4* mtiles,
                                                           int32_t* nmtiles) {
@@ -618,7 +634,7 @@ __global__ void __launch_bounds__(1024) gemm_tiles_kernel(const int32_t* __restr
   const int per = (E + 1023) / 1024;
   const int e0 = threadIdx.x * per;
   int local = 0;
-  for (int e = e0; e < min(E, e0 + per); ++e) local += (counts[e] + kBM - 1) / kBM;
+  for (int e = e0; e < min(E, e0 + per); ++e) local += (counts[e] + 2 * kBM - 1) / (2 * kBM);
   // block exclusive scan
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int incl = local;
@@ -640,7 +656,8 @@ __global__ void __launch_bounds__(1024) gemm_tiles_kernel(const int32_t* __restr
   int start = incl - local + (warp > 0 ? wsum[warp - 1] : 0);
   for (int e = e0; e < min(E, e0 + per); ++e) {
     const int c = counts[e], o = offsets[e];
-    for (int r0 = 0; r0 < c; r0 += kBM) mtiles[start++] = make_int4(e, o + r0, min(kBM, c - r0), 0);
+    for (int r0 = 0; r0 < c; r0 += 2 * kBM)
+      mtiles[start++] = make_int4(e, o + r0, min(kBM, c - r0), max(0, min(kBM, c - r0 - kBM)));
   }
   if (threadIdx.x == 1023) *nmtiles = start;
 }
@@ -782,7 +799,7 @@ cudaError_t launch_router_tc(const uint16_t* x, int T, int d, int E, const uint1
   cudaError_t e = activation_map(&ma, x, d, T, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
   if (e == cudaSuccess) e = activation_map(&mb, wsplit, 2 * d, E, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
   if (e != cudaSuccess) return e;
-  const int items = (T + kBM - 1) / kBM * ((E + 127) / 128);
+  const int items = (T + 2 * kBM - 1) / (2 * kBM) * ((E + 127) / 128);
   return launch_gemm_mode<2>(ma, mb, g, items < num_sms ? items : num_sms, s);
 }
 

@@ -22,7 +22,8 @@ namespace k3 {
 namespace {
 
 constexpr int kRouterWarps = 8;  // 2 warps per expert row (each half of d)
-constexpr int kRowsPerCta = kRouterWarps / 2;
+constexpr int kWarpsPerRow = 2;
+constexpr int kRowsPerCta = kRouterWarps / kWarpsPerRow;
 constexpr int kTokTile = 4;      // tokens staged in shared memory at a time
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
@@ -49,6 +50,8 @@ __device__ void stage_tokens(const RouterArgs& a, int t0, int nt, uint16_t* xs) 
 }
 
 // x row (bf16, in shared memory) -> fp16 B-fragment row with a per-token power-of-two scale.
+// Every CTA computes the same max (same data, same reduction order) and converts only its
+// share of the row's fragment items; CTA 0 records the scale.
 __device__ void convert_token(const RouterArgs& a, int t, const uint16_t* xr, float* red) {
   float m = 0.f;
   for (int j = threadIdx.x * 2; j < a.d; j += blockDim.x * 2) {
@@ -61,10 +64,13 @@ __device__ void convert_token(const RouterArgs& a, int t, const uint16_t* xr, fl
   __syncthreads();
   m = red[0];
   for (int i = 1; i < (int)(blockDim.x >> 5); ++i) m = fmaxf(m, red[i]);
+  __syncthreads();  // red is reused by the next token
   const int q = fp16_scale_exp(m);
   const float inv = exp2i(-q);
   const int items = (a.d / 32) * 4;
-  for (int it = threadIdx.x; it < items; it += blockDim.x) {
+  const int per = (items + (int)gridDim.x - 1) / (int)gridDim.x;
+  const int i0 = min(items, (int)blockIdx.x * per), i1 = min(items, i0 + per);
+  for (int it = i0 + (int)threadIdx.x; it < i1; it += blockDim.x) {
     const int blk = it >> 2, tq = it & 3;
     __align__(16) __half h[8];
 #pragma unroll
@@ -79,27 +85,25 @@ __device__ void convert_token(const RouterArgs& a, int t, const uint16_t* xr, fl
     }
     *reinterpret_cast<uint4*>(a.ws.xfrag + (size_t)t * a.d + (size_t)it * 8) = *reinterpret_cast<uint4*>(h);
   }
-  if (threadIdx.x == 0) a.ws.xscale[t] = exp2i(q);
-  __syncthreads();
+  if (blockIdx.x == 0 && threadIdx.x == 0) a.ws.xscale[t] = exp2i(q);
 }
 
 // --------------------------------------------------------------------------- logits ---
-// CTA = kRowsPerCta expert rows; warp w handles row w/2, half w%2 of d; the two halves are added
-// in a fixed order.  Tokens are staged kTokTile at a time; the CTA with blockIdx == t % grid
-// also converts token t to fp16 fragments.
-__device__ void logits_and_convert(const RouterArgs& a, uint16_t* xs, float* red, float* half_sum) {
+// CTA = kRowsPerCta expert rows; warp w handles row w / kWarpsPerRow, part w % kWarpsPerRow of
+// d; the partial sums are added in a fixed order.  Tokens are staged kTokTile at a time; every CTA converts its
+// share of each token to fp16 fragments.
+__device__ void logits_and_convert(const RouterArgs& a, uint16_t* xs, float* red, float* part) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = blockIdx.x * kRowsPerCta + (warp >> 1);
-  const int hf = warp & 1;
-  const int nq = a.d / 4, q0 = hf * (nq / 2), q1 = q0 + nq / 2;
+  const int e = blockIdx.x * kRowsPerCta + warp / kWarpsPerRow;
+  const int qt = warp % kWarpsPerRow;
+  const int nq = a.d / 4, span = nq / kWarpsPerRow, q0 = qt * span, q1 = q0 + span;
   const float4* wr = reinterpret_cast<const float4*>(a.Wr + (size_t)(e < a.E ? e : 0) * a.d);
   for (int t0 = 0; t0 < a.T; t0 += kTokTile) {
     const int nt = min(kTokTile, a.T - t0);
     __syncthreads();
     stage_tokens(a, t0, nt, xs);
     __syncthreads();
-    for (int tt = 0; tt < nt; ++tt)
-      if ((t0 + tt) % (int)gridDim.x == (int)blockIdx.x) convert_token(a, t0 + tt, xs + (size_t)tt * a.d, red);
+    for (int tt = 0; tt < nt; ++tt) convert_token(a, t0 + tt, xs + (size_t)tt * a.d, red);
     float acc[kTokTile] = {0.f, 0.f, 0.f, 0.f};
     if (e < a.E) {
       constexpr int kB = 14;  // W_r loads in flight per lane
@@ -133,11 +137,16 @@ __device__ void logits_and_convert(const RouterArgs& a, uint16_t* xs, float* red
       float v = acc[tt];
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-      if (lane == 0) half_sum[warp * kTokTile + tt] = v;
+      if (lane == 0) part[warp * kTokTile + tt] = v;
     }
     __syncthreads();
-    if (hf == 0 && lane < nt && e < a.E)
-      a.ws.logits[(size_t)(t0 + lane) * a.E + e] = half_sum[warp * kTokTile + lane] + half_sum[(warp + 1) * kTokTile + lane];
+    if (qt == 0 && lane < nt && e < a.E) {
+      const float* pp = part + warp * kTokTile + lane;
+      float v = pp[0];
+#pragma unroll
+      for (int h = 1; h < kWarpsPerRow; ++h) v += pp[h * kTokTile];
+      a.ws.logits[(size_t)(t0 + lane) * a.E + e] = v;
+    }
   }
 }
 
@@ -445,6 +454,74 @@ __device__ void bucket_block(const int32_t* idx, int P, int k, int E, int32_t* c
   }
 }
 
+// Bucketing of a few picks (P <= blockDim, at most kUnitTokens picks per expert), all in
+// shared memory: the same counts, offsets, stable perm, active list and work units as
+// bucket_block.  The rank of pick p is the number of picks with a lower expert id, or the same
+// expert and a lower pick id; each run of equal experts in rank order is one unit.
+__device__ void bucket_small(const int32_t* sidx, const float* sw, int P, int k, int E, int32_t* counts,
+                             int32_t* offsets, int32_t* perm, int32_t* act, int32_t* nact, UnitDesc* units,
+                             int32_t* nunits, const float* xscale, int* smem) {
+  int* sperm = smem;      // [P] pick at rank r
+  int* sel = smem + P;    // [P] expert at rank r
+  const int tid = threadIdx.x;
+  if (tid < P) {
+    const int e = sidx[tid];
+    int r = 0;
+    for (int q = 0; q < P; ++q) {
+      const int eq = sidx[q];
+      r += (eq < e) || (eq == e && q < tid);
+    }
+    sperm[r] = tid;
+    sel[r] = e;
+  }
+  __syncthreads();
+  const bool start = tid < P && (tid == 0 || sel[tid - 1] != sel[tid]);
+  const int nd = __syncthreads_count(start);
+  if (tid < P) {
+    perm[tid] = sperm[tid];
+    if (start) {
+      int g = 0;
+      for (int q = 1; q <= tid; ++q) g += sel[q - 1] != sel[q];
+      int M = 1;
+      while (tid + M < P && sel[tid + M] == sel[tid]) ++M;
+      act[g] = sel[tid];
+      UnitDesc& U = units[g];
+      U.e = sel[tid];
+      U.M = M;
+      U.pbase = tid;
+      U.pad = 0;
+#pragma unroll
+      for (int m = 0; m < kUnitTokens; ++m) {
+        const int pk = m < M ? sperm[tid + m] : -1;
+        const int t = m < M ? pk / k : 0;
+        U.pick[m] = pk;
+        U.tok[m] = t;
+        U.xs[m] = m < M ? __ldcg(xscale + t) : 0.f;
+        U.w[m] = m < M ? sw[pk] : 0.f;
+      }
+    }
+  }
+  for (int e = tid; e < E; e += blockDim.x) {
+    int lo = 0, hi = P;  // first rank with expert >= e
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (sel[mid] < e) lo = mid + 1; else hi = mid;
+    }
+    int lo2 = lo, hi2 = P;  // first rank with expert > e
+    while (lo2 < hi2) {
+      const int mid = (lo2 + hi2) >> 1;
+      if (sel[mid] <= e) lo2 = mid + 1; else hi2 = mid;
+    }
+    offsets[e] = lo;
+    counts[e] = lo2 - lo;
+  }
+  if (tid == 0) {
+    offsets[E] = P;
+    *nact = nd;
+    *nunits = nd;
+  }
+}
+
 namespace {
 
 __host__ inline size_t fused_select_smem(int E, int P) {
@@ -454,10 +531,10 @@ __host__ inline size_t fused_select_smem(int E, int P) {
 __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(RouterArgs a) {
   extern __shared__ __align__(16) uint8_t rsm[];
   __shared__ float red[kRouterWarps];
-  __shared__ float half_sum[kRouterWarps * kTokTile];
+  __shared__ float part[kRouterWarps * kTokTile];
   __shared__ int last;
   pdl_entry();
-  logits_and_convert(a, reinterpret_cast<uint16_t*>(rsm), red, half_sum);
+  logits_and_convert(a, reinterpret_cast<uint16_t*>(rsm), red, part);
   if (!a.fuse_select) return;
   __threadfence();
   __syncthreads();
@@ -476,8 +553,12 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(RouterArgs a)
   for (int t = 0; t < a.T; ++t)
     topk_block(a.ws.logits + (size_t)t * a.E, a.bias, a.E, a.k, ku, sg, cand, a.ws.idx + (size_t)t * a.k,
                a.ws.w + (size_t)t * a.k, sidx + (size_t)t * a.k, sw + (size_t)t * a.k);
-  bucket_block(sidx, P, a.k, a.E, a.ws.counts, a.ws.offsets, a.ws.perm, a.ws.act, a.ws.nact, a.ws.units,
-               a.ws.nunits, sw, a.ws.xscale, bsm, true, true);
+  if (P <= (int)blockDim.x && a.T <= kUnitTokens)
+    bucket_small(sidx, sw, P, a.k, a.E, a.ws.counts, a.ws.offsets, a.ws.perm, a.ws.act, a.ws.nact, a.ws.units,
+                 a.ws.nunits, a.ws.xscale, bsm);
+  else
+    bucket_block(sidx, P, a.k, a.E, a.ws.counts, a.ws.offsets, a.ws.perm, a.ws.act, a.ws.nact, a.ws.units,
+                 a.ws.nunits, sw, a.ws.xscale, bsm, true, true);
   if (threadIdx.x == 0) a.ws.sync[0] = 0u;
 }
 
@@ -506,7 +587,7 @@ __global__ void __launch_bounds__(1024) bucket_kernel(const int32_t* idx, int P,
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s) {
   // dynamic shared memory: the staged token tile, reused by the last block for top-k keys
   // (kRouterWarps * E floats) and bucketing (2 * E ints)
-  size_t smem = (size_t)kTokTile * a.d * sizeof(uint16_t);
+  size_t smem = (size_t)std::min(a.T, kTokTile) * a.d * sizeof(uint16_t);
   if (a.fuse_select) smem = std::max(smem, fused_select_smem(a.E, a.T * a.k));
   static bool attr = false;
   if (!attr) {
