@@ -50,8 +50,6 @@ __device__ void stage_tokens(const RouterArgs& a, int t0, int nt, uint16_t* xs) 
 }
 
 // x row (bf16, in shared memory) -> fp16 B-fragment row with a per-token power-of-two scale.
-// Every CTA computes the same max (same data, same reduction order) and converts only its
-// share of the row's fragment items; CTA 0 records the scale.
 __device__ void convert_token(const RouterArgs& a, int t, const uint16_t* xr, float* red) {
   float m = 0.f;
   for (int j = threadIdx.x * 2; j < a.d; j += blockDim.x * 2) {
@@ -64,13 +62,10 @@ __device__ void convert_token(const RouterArgs& a, int t, const uint16_t* xr, fl
   __syncthreads();
   m = red[0];
   for (int i = 1; i < (int)(blockDim.x >> 5); ++i) m = fmaxf(m, red[i]);
-  __syncthreads();  // red is reused by the next token
   const int q = fp16_scale_exp(m);
   const float inv = exp2i(-q);
   const int items = (a.d / 32) * 4;
-  const int per = (items + (int)gridDim.x - 1) / (int)gridDim.x;
-  const int i0 = min(items, (int)blockIdx.x * per), i1 = min(items, i0 + per);
-  for (int it = i0 + (int)threadIdx.x; it < i1; it += blockDim.x) {
+  for (int it = threadIdx.x; it < items; it += blockDim.x) {
     const int blk = it >> 2, tq = it & 3;
     __align__(16) __half h[8];
 #pragma unroll
@@ -85,13 +80,14 @@ __device__ void convert_token(const RouterArgs& a, int t, const uint16_t* xr, fl
     }
     *reinterpret_cast<uint4*>(a.ws.xfrag + (size_t)t * a.d + (size_t)it * 8) = *reinterpret_cast<uint4*>(h);
   }
-  if (blockIdx.x == 0 && threadIdx.x == 0) a.ws.xscale[t] = exp2i(q);
+  if (threadIdx.x == 0) a.ws.xscale[t] = exp2i(q);
+  __syncthreads();
 }
 
 // --------------------------------------------------------------------------- logits ---
 // CTA = kRowsPerCta expert rows; warp w handles row w / kWarpsPerRow, part w % kWarpsPerRow of
-// d; the partial sums are added in a fixed order.  Tokens are staged kTokTile at a time; every CTA converts its
-// share of each token to fp16 fragments.
+// d; the partial sums are added in a fixed order.  Tokens are staged kTokTile at a time; the CTA
+// with blockIdx == t % grid also converts token t to fp16 fragments.
 __device__ void logits_and_convert(const RouterArgs& a, uint16_t* xs, float* red, float* part) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * kRowsPerCta + warp / kWarpsPerRow;
@@ -103,7 +99,8 @@ __device__ void logits_and_convert(const RouterArgs& a, uint16_t* xs, float* red
     __syncthreads();
     stage_tokens(a, t0, nt, xs);
     __syncthreads();
-    for (int tt = 0; tt < nt; ++tt) convert_token(a, t0 + tt, xs + (size_t)tt * a.d, red);
+    for (int tt = 0; tt < nt; ++tt)
+      if ((t0 + tt) % (int)gridDim.x == (int)blockIdx.x) convert_token(a, t0 + tt, xs + (size_t)tt * a.d, red);
     float acc[kTokTile] = {0.f, 0.f, 0.f, 0.f};
     if (e < a.E) {
       constexpr int kB = 14;  // W_r loads in flight per lane
