@@ -656,20 +656,29 @@ __global__ void __launch_bounds__(kDnThreads, 2) down_kernel(FfnArgs a, DnLayout
 }
 
 // ------------------------------------------------------------------------- combine ---
-__global__ void __launch_bounds__(64) combine_kernel(const float* __restrict__ obuf, int T, int d, int k,
-                                                      float* __restrict__ y) {
+// y[t][c] = sum over slots 0..k-1, in slot order, of obuf[t*k + slot][c].  A thread owns 4
+// columns; its slot loads are issued 8 at a time before any is added.
+__global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ obuf, int T, int d, int k,
+                                                       float* __restrict__ y) {
   pdl_entry();
   const size_t n4 = (size_t)T * d / 4;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
     const size_t t = i / (d / 4), c4 = i % (d / 4);
     const float4* src = reinterpret_cast<const float4*>(obuf + (size_t)t * k * d) + c4;
-    float4 acc = __ldg(src);
-    for (int slot = 1; slot < k; ++slot) {
-      const float4 v = __ldg(src + (size_t)slot * (d / 4));
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < k; s0 += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = s0 + j < k ? __ldg(src + (size_t)(s0 + j) * (d / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (s0 + j < k) {
+          acc.x = (s0 + j == 0) ? v[j].x : acc.x + v[j].x;
+          acc.y = (s0 + j == 0) ? v[j].y : acc.y + v[j].y;
+          acc.z = (s0 + j == 0) ? v[j].z : acc.z + v[j].z;
+          acc.w = (s0 + j == 0) ? v[j].w : acc.w + v[j].w;
+        }
+      }
     }
     reinterpret_cast<float4*>(y)[i] = acc;
   }
@@ -751,8 +760,8 @@ cudaError_t launch_down(const FfnArgs& a, cudaStream_t s) {
 
 cudaError_t launch_combine(const FfnArgs& a, cudaStream_t s) {
   const size_t n4 = (size_t)a.T * a.d / 4;
-  const int grid = (int)std::min<size_t>((n4 + 63) / 64, (size_t)a.num_sms * 32);
-  return launch_pdl(combine_kernel, dim3(grid), dim3(64), 0, s, (const float*)a.ws.obuf, a.T, a.d, a.k, a.y);
+  const int grid = (int)std::min<size_t>((n4 + 127) / 128, (size_t)a.num_sms * 16);
+  return launch_pdl(combine_kernel, dim3(grid), dim3(128), 0, s, (const float*)a.ws.obuf, a.T, a.d, a.k, a.y);
 }
 
 }  // namespace k3
