@@ -140,6 +140,32 @@ def _traffic_from_profile(kernel_file: str, summary: str):
         return None
 
 
+# ------------------------------------------------------------------ replica aggregation ---
+
+def job_throughput(units_per_rank: float, ms_rank: float, pg=None, device: str = "cuda"):
+    """Whole-job rate over replicas: every rank processed units_per_rank in ms_rank; the job
+    took as long as its slowest rank.  Returns (units of all ranks per second, max ms)."""
+    ms = ms_rank
+    ws = 1
+    if pg is not None:
+        import torch
+        ws = pg.get_world_size()
+        t = torch.tensor([ms_rank], dtype=torch.float64, device=device)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    return units_per_rank * ws / (ms / 1e3), ms
+
+
+def job_rate_min(rate_rank: float, pg=None, device: str = "cuda") -> float:
+    """Whole-job rate when each rank measured its own rate: the slowest rank's rate x ranks."""
+    if pg is None:
+        return rate_rank
+    import torch
+    t = torch.tensor([rate_rank], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MIN)
+    return float(t.item()) * pg.get_world_size()
+
+
 # --------------------------------------------------------------------------- b300 arm ---
 
 def build_layer(torch, k3, T_max, bias=None, n_exp=E):
@@ -215,12 +241,7 @@ def run_b300(args):
     prof = k3.k3moe_profile_read(layer)
     k3.k3moe_profile(layer, False)
     clk = clocks.stop()
-    if pg:
-        t = torch.tensor([ms], device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
-    tokens = tokens_per_step * args.steps * ws
-    value = tokens / (ms / 1e3)
+    value, ms = job_throughput(tokens_per_step * args.steps, ms, pg)
 
     # distinct experts touched (algorithmic weight bytes): counted from the actual routing
     idx = torch.empty((tokens_per_step, K), dtype=torch.int32, device="cuda")
@@ -279,11 +300,7 @@ def run_b300(args):
         for c in range(calls):
             k3.k3moe_layer_forward_host(layer, xh[c * T:(c + 1) * T], T, yh[c * T:(c + 1) * T], stream)
     e2e_s = time.perf_counter() - t0
-    e2e_val = tokens_per_step * e2e_steps / e2e_s
-    if pg:
-        t = torch.tensor([e2e_val], device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MIN)
-        e2e_val = float(t.item()) * ws
+    e2e_val = job_rate_min(tokens_per_step * e2e_steps / e2e_s, pg)
 
     out = None
     if rank == 0:
@@ -401,11 +418,7 @@ def run_stack4(args):
             a[0] += kms
             a[1] += kn
         k3.k3moe_profile(L, False)
-    if pg:
-        t = torch.tensor([ms], device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
-    value = n_tok * args.steps * ws / (ms / 1e3)
+    value, ms = job_throughput(n_tok * args.steps, ms, pg)
     hbm_peak, _, peak_kind = _peaks()
     gu_ms, gu_n = prof.get("gateup", (0.0, 0))
     achieved = K * GATEUP_BYTES / (gu_ms / gu_n / 1e3) / 1e9 if gu_n else None
