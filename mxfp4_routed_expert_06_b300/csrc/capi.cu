@@ -225,6 +225,7 @@ cudaError_t reset_after_timeout(k3moe_layer* L) {
   const k3moe_dims& D = L->dims;
   cudaError_t e = cudaMemset(L->ws.sync, 0, 64);
   if (e == cudaSuccess) e = cudaMemset(L->ws.pair, 0, (size_t)D.T_max * D.k * (D.f / 32) * 4);
+  if (e == cudaSuccess) e = cudaMemset(L->ws.hmax, 0, (size_t)D.T_max * D.k * 4);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   return e;
 }
@@ -397,6 +398,8 @@ int forward_impl(k3moe_layer* L, const void* x, int T, float* y, cudaStream_t s)
              L->zero_scales ? 1 : 0};
   L->test_stall = 0;
   rc = timed_launch(L, KID_GATEUP, s, [&] { return launch_gateup(fa, s); });
+  if (rc) return rc;
+  rc = timed_launch(L, KID_GATHER, s, [&] { return launch_hconv(fa, s); });
   if (rc) return rc;
   rc = timed_launch(L, KID_DOWN, s, [&] { return launch_down(fa, s); });
   if (rc) return rc;

@@ -19,11 +19,12 @@
 //   gateup_kernel  task = (unit, 16 rows of f); stage = one 128-column k-tile of the gate and
 //                  up tiles (2176 B) + the unit's x fragments for it; consumer warp w takes
 //                  k-tiles kt % 8 == w; one of 4 epilogue warps adds the 8 partial sums in
-//                  warp order, applies SwiGLU h = silu(g) * u, and the second of the two 16-row
-//                  halves of a 32-row block to finish converts that block of h to fp16
-//                  fragments with one power-of-two scale per (pick, 32 rows).
+//                  warp order, applies SwiGLU h = silu(g) * u, writes h (fp32) and records
+//                  max |h| per pick.
+//   hconv_kernel   h -> fp16 B fragments with one power-of-two scale per pick (fp16 never
+//                  overflows; the scale factors out of the down projection's sum).
 //   down_kernel    task = (unit, 16 rows of d) over the whole f range, streamed in chunks of
-//                  k-tiles; consumer warp = task % 8; writes w * o to obuf[pick].
+//                  k-tiles; consumer warp = task % 8; writes w * hs * o to obuf[pick].
 //   combine_kernel y[t] = sum over the k slots, in slot order, of obuf[t*k + slot].
 // Every device-side wait is bounded (globaltimer); on expiry the kernel sets an error flag
 // that the host reads at its next synchronisation, drains its copies in flight and returns.
@@ -390,7 +391,6 @@ __global__ void __launch_bounds__(kGuThreads, 2) gateup_kernel(FfnArgs a, GuLayo
   {
     const int ew = warp - kConsumers;  // 0..kGuEpi-1: tasks j with j % kGuEpi == ew
     const int g = lane >> 2, t = lane & 3;
-    const int nblk = a.f / 32;
     int j = ew;
     int i = blockIdx.x + ew * G;
     // lane m < 8 holds pick m and its x scale of the task's unit; prefetched a task ahead
@@ -425,8 +425,8 @@ __global__ void __launch_bounds__(kGuThreads, 2) gateup_kernel(FfnArgs a, GuLayo
       if (lane == 0) mbar_arrive(&red_empty[r]);
 
       const int rg = i % RG;
-      const int blk = rg >> 1;
       // SwiGLU for this lane's entries: rows 16rg+g (+8), columns (picks) 2t, 2t+1
+      float hmx[2] = {0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const int n = 2 * t + c;
@@ -438,51 +438,52 @@ __global__ void __launch_bounds__(kGuThreads, 2) gateup_kernel(FfnArgs a, GuLayo
             const float gv = v[0 * 4 + 2 * h + c] * xs, uv = v[1 * 4 + 2 * h + c] * xs;
             const float hv = gv / (1.0f + expf(-gv)) * uv;
             a.ws.hbuf[(size_t)p * a.f + rg * kTileRows + g + 8 * h] = hv;
+            hmx[c] = fmaxf(hmx[c], fabsf(hv));
           }
         }
       }
-      __syncwarp();
-      // the second of the two 16-row halves of a 32-row block converts it, per pick: lane m's
-      // acq_rel increment publishes this warp's h rows and, on the second arrival, makes the
-      // other half's rows visible
-      int last = 0;
-      if (lane < M) {
-        int old;
-        asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;"
-                     : "=r"(old)
-                     : "l"(a.ws.pair + (size_t)mypick * nblk + blk)
-                     : "memory");
-        last = old == 1;
-      }
-      unsigned todo = __ballot_sync(0xffffffffu, last);
-      while (todo) {
-        const int m = __ffs(todo) - 1;
-        todo &= todo - 1;
-        const int p = __shfl_sync(0xffffffffu, mypick, m);
-        const float hv = __ldcg(a.ws.hbuf + (size_t)p * a.f + blk * 32 + lane);
-        float mx = fabsf(hv);
+      // max |h| per pick over this task's 16 rows: reduce over the 8 row lanes of each column,
+      // then one atomic per (task, pick); hconv_kernel turns it into the pick's fp16 scale
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        const int q = fp16_scale_exp(mx);
-        const uint16_t hb = __half_as_ushort(__float2half_rn(hv * exp2i(-q)));
-        // lane tq < 4 gathers rows 16s + 2tq + {0, 1, 8, 9} (s = 0, 1) of the block
-        __align__(16) uint16_t frag[8];
+      for (int c = 0; c < 2; ++c) {
+        const int n = 2 * t + c;
+        const int p = __shfl_sync(0xffffffffu, mypick, n);
+        float m = n < M ? hmx[c] : 0.f;
 #pragma unroll
-        for (int s2 = 0; s2 < 2; ++s2) {
-          const int base = 16 * s2 + 2 * (lane & 3);
-          frag[4 * s2 + 0] = (uint16_t)__shfl_sync(0xffffffffu, (int)hb, base);
-          frag[4 * s2 + 1] = (uint16_t)__shfl_sync(0xffffffffu, (int)hb, base + 1);
-          frag[4 * s2 + 2] = (uint16_t)__shfl_sync(0xffffffffu, (int)hb, base + 8);
-          frag[4 * s2 + 3] = (uint16_t)__shfl_sync(0xffffffffu, (int)hb, base + 9);
-        }
-        if (lane < 4)
-          *reinterpret_cast<uint4*>(a.ws.hfrag + (size_t)p * a.f + (size_t)(blk * 4 + lane) * 8) =
-              *reinterpret_cast<const uint4*>(frag);
-        if (lane == 0) {
-          a.ws.hscale[(size_t)p * nblk + blk] = exp2i(q);
-          a.ws.pair[(size_t)p * nblk + blk] = 0;
-        }
+        for (int off = 4; off < 32; off <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        if (g == 0 && n < M) atomicMax(a.ws.hmax + p, __float_as_uint(m));
       }
+    }
+  }
+}
+
+// --------------------------------------------------------------------------- hconv ---
+// h (fp32, [P][f]) -> fp16 B-fragment rows with one power of two per pick (h = hfrag * hs[p]),
+// from the max |h| that gateup_kernel recorded; the max is reset to zero for the next call.
+__global__ void __launch_bounds__(128) hconv_kernel(const float* __restrict__ hbuf, uint32_t* hmax, int f, int P,
+                                                     __half* __restrict__ hfrag, float* __restrict__ hs) {
+  pdl_entry();
+  for (int p = blockIdx.x; p < P; p += gridDim.x) {
+    const int q = fp16_scale_exp(__uint_as_float(hmax[p]));
+    const float inv = exp2i(-q);
+    const float* hr = hbuf + (size_t)p * f;
+    for (int it = threadIdx.x; it < f / 8; it += blockDim.x) {
+      const int blk = it >> 2, tq = it & 3;
+      __align__(16) __half h[8];
+#pragma unroll
+      for (int s2 = 0; s2 < 2; ++s2) {
+        const int kb = 32 * blk + 16 * s2 + 2 * tq;
+        h[4 * s2 + 0] = __float2half_rn(hr[kb] * inv);
+        h[4 * s2 + 1] = __float2half_rn(hr[kb + 1] * inv);
+        h[4 * s2 + 2] = __float2half_rn(hr[kb + 8] * inv);
+        h[4 * s2 + 3] = __float2half_rn(hr[kb + 9] * inv);
+      }
+      *reinterpret_cast<uint4*>(hfrag + (size_t)p * f + (size_t)it * 8) = *reinterpret_cast<const uint4*>(h);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      hs[p] = exp2i(q);
+      hmax[p] = 0u;
     }
   }
 }
@@ -500,7 +501,7 @@ struct DnLayout {
 inline DnLayout dn_layout(int f, int mcap, size_t budget) {
   DnLayout L;
   const int KT = f / kTileCols;
-  const size_t per_kt = kTileBytes + (size_t)mcap * (4 * 64 + 4 * 4);  // weights + h fragments + h scales
+  const size_t per_kt = kTileBytes + (size_t)mcap * (4 * 64);  // weights + h fragments
   int kc = (int)(budget / ((size_t)kConsumers * 3 * per_kt));           // aim for 3 stages per warp
   kc = kc < 1 ? 1 : (kc > KT ? KT : kc);
   L.kc = kc;
@@ -541,10 +542,9 @@ __global__ void __launch_bounds__(kDnThreads, 2) down_kernel(FfnArgs a, DnLayout
   const int KT = a.f / kTileCols;
   const int ntasks = *a.ws.nunits * RG;
   const size_t gu_bytes = gateup_region_bytes(a.d, a.f);
-  const int nblk = a.f / 32;
   const int wb = L.kc * kTileBytes;  // weight bytes of a full chunk
   const int G = gridDim.x;
-  // stage: [kc weight tiles][M x kc*256 h fragments][M x kc*16 h scales]
+  // stage: [kc weight tiles][M x kc*256 h fragments]
   uint8_t* ring = smem + (size_t)warp * L.depth * L.stage_bytes;
   const uint64_t pol_w = policy_evict_first(), pol_h = policy_evict_normal();
   const int first = blockIdx.x + warp * G, step = kConsumers * G;
@@ -567,8 +567,6 @@ __global__ void __launch_bounds__(kDnThreads, 2) down_kernel(FfnArgs a, DnLayout
       const int p = d_pick(dcur, m);
       warp_copy(st + wb + m * L.kc * 256, reinterpret_cast<const uint8_t*>(a.ws.hfrag + (size_t)p * a.f) + kt0 * 256,
                 nk * 256, lane, pol_h);
-      warp_copy(st + wb + M * L.kc * 256 + m * L.kc * 16,
-                reinterpret_cast<const uint8_t*>(a.ws.hscale + (size_t)p * nblk) + kt0 * 16, nk * 16, lane, pol_h);
     }
     if (++ci == L.nch) {
       ci = 0;
@@ -598,16 +596,12 @@ __global__ void __launch_bounds__(kDnThreads, 2) down_kernel(FfnArgs a, DnLayout
     if (j + 1 < my_tasks) dtask = load_desc(a.ws.units + (i + step) / RG, lane);
     const int M = d_M(D);
     const int rg = i % RG;
-    const int n0 = 2 * t, n1 = 2 * t + 1;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int c = 0; c < L.nch; ++c) {
       cp_wait<DEPTH - 1>();
       __syncwarp();
       uint8_t* st = ring + (size_t)rslot * L.stage_bytes;
       const uint8_t* hrow = st + wb + g * L.kc * 256;
-      const float* hs = reinterpret_cast<const float*>(st + wb + M * L.kc * 256);
-      const float* hs0 = hs + (n0 < M ? n0 : 0) * L.kc * 4;
-      const float* hs1 = hs + (n1 < M ? n1 : 0) * L.kc * 4;
       const int nk = min(L.kc, KT - c * L.kc);
       for (int kk = 0; kk < nk; ++kk) {
         const uint8_t* tp = st + (size_t)kk * kTileBytes;
@@ -625,12 +619,10 @@ __global__ void __launch_bounds__(kDnThreads, 2) down_kernel(FfnArgs a, DnLayout
           mma_acc(bacc, A, hv.z, hv.w);
           const float s_lo = scale_of<ZS>(sc.x, b);
           const float s_hi = scale_of<ZS>(sc.y, b);
-          const float h0 = n0 < M ? hs0[4 * kk + b] : 0.f;
-          const float h1 = n1 < M ? hs1[4 * kk + b] : 0.f;
-          acc[0] = fmaf(bacc[0], s_lo * h0, acc[0]);
-          acc[1] = fmaf(bacc[1], s_lo * h1, acc[1]);
-          acc[2] = fmaf(bacc[2], s_hi * h0, acc[2]);
-          acc[3] = fmaf(bacc[3], s_hi * h1, acc[3]);
+          acc[0] = fmaf(bacc[0], s_lo, acc[0]);
+          acc[1] = fmaf(bacc[1], s_lo, acc[1]);
+          acc[2] = fmaf(bacc[2], s_hi, acc[2]);
+          acc[3] = fmaf(bacc[3], s_hi, acc[3]);
         }
       }
       __syncwarp();
@@ -647,8 +639,9 @@ __global__ void __launch_bounds__(kDnThreads, 2) down_kernel(FfnArgs a, DnLayout
       const int p = d_pick(D, n);
       const float wp = d_w(D, n);
       if (n < M) {
-        a.ws.obuf[(size_t)p * a.d + rg * kTileRows + g] = acc[c] * wp;
-        a.ws.obuf[(size_t)p * a.d + rg * kTileRows + g + 8] = acc[2 + c] * wp;
+        const float sc = wp * __ldg(a.ws.hscale + p);  // combine weight x the pick's h scale
+        a.ws.obuf[(size_t)p * a.d + rg * kTileRows + g] = acc[c] * sc;
+        a.ws.obuf[(size_t)p * a.d + rg * kTileRows + g + 8] = acc[2 + c] * sc;
       }
     }
   }
@@ -756,6 +749,12 @@ cudaError_t launch_down(const FfnArgs& a, cudaStream_t s) {
     case 4: return zs ? launch_dn<4, true>(a, L, s) : launch_dn<4, false>(a, L, s);
     default: return zs ? launch_dn<6, true>(a, L, s) : launch_dn<6, false>(a, L, s);
   }
+}
+
+cudaError_t launch_hconv(const FfnArgs& a, cudaStream_t s) {
+  const int P = a.T * a.k;
+  return launch_pdl(hconv_kernel, dim3(std::min(P, a.num_sms * 8)), dim3(128), 0, s, (const float*)a.ws.hbuf,
+                    a.ws.hmax, a.f, P, a.ws.hfrag, a.ws.hscale);
 }
 
 cudaError_t launch_combine(const FfnArgs& a, cudaStream_t s) {

@@ -663,15 +663,19 @@ __global__ void __launch_bounds__(1024) gemm_tiles_kernel(const int32_t* __restr
 }
 
 // h fp32 -> h16 fp16 with one power of two per row (h = h16 * hs[row])
-__global__ void __launch_bounds__(256) gemm_h16_kernel(const float* __restrict__ hbuf,
-                                                       const uint32_t* __restrict__ hmax, int f, __half* h16,
+__global__ void __launch_bounds__(256) gemm_h16_kernel(const float* __restrict__ hbuf, uint32_t* hmax, int f,
+                                                       __half* h16,
                                                        float* hs) {
   pdl_entry();
   const size_t base = (size_t)blockIdx.x * f;
   const int q = fp16_scale_exp(__uint_as_float(hmax[blockIdx.x]));
   const float inv = exp2i(-q);
   for (int j = threadIdx.x; j < f; j += 256) h16[base + j] = __float2half_rn(hbuf[base + j] * inv);
-  if (threadIdx.x == 0) hs[blockIdx.x] = exp2i(q);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    hs[blockIdx.x] = exp2i(q);
+    hmax[blockIdx.x] = 0u;  // zero between calls (the register-decode path also accumulates into it)
+  }
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -769,8 +773,7 @@ cudaError_t launch_gemm_gu(const GemmFfn& q, cudaStream_t s) {
 }
 
 cudaError_t launch_gemm_h16(const GemmFfn& q, int P, cudaStream_t s) {
-  return launch_pdl(gemm_h16_kernel, dim3(P), dim3(256), 0, s, (const float*)q.hbuf, (const uint32_t*)q.hmax, q.f,
-                    q.h16, q.hs);
+  return launch_pdl(gemm_h16_kernel, dim3(P), dim3(256), 0, s, (const float*)q.hbuf, q.hmax, q.f, q.h16, q.hs);
 }
 
 cudaError_t launch_gemm_dn(const GemmFfn& q, cudaStream_t s) {

@@ -78,16 +78,17 @@ struct Workspace {
   UnitDesc* units = nullptr;    // [P/8 + E] work units
   int32_t* nunits = nullptr;    // [1]
   float* hbuf = nullptr;        // [P][f] SwiGLU output, fp32
-  int32_t* pair = nullptr;      // [P][f/32] halves of a 32-row block written (kept at zero between calls)
+  int32_t* pair = nullptr;      // [P][f/32] (unused since h has one scale per pick; kept zero)
   __half* hfrag = nullptr;      // [P][f] fragment order
-  float* hscale = nullptr;      // [P][f/32] power of two per (pick, 32-block)
+  float* hscale = nullptr;      // [P] power of two per pick (h = hfrag * hscale); sized [P][f/32]
   float* obuf = nullptr;        // [P][d] w-scaled expert outputs
   uint32_t* sync = nullptr;     // [16]: [0] router last-block ticket, [1] device error flags
   int32_t* bad = nullptr;       // [4] pack time: [0] error flags, [1] min scale byte, [2] max scale byte
   // tensor-core path (large T); it also reuses obuf (first as xg, the fp16 rows of x in bucketed
   // order [P][d], which the down projection then overwrites), hbuf (fp32 h [P][f]), hfrag (as
   // h16 [P][f]) and hscale (as the per-row power of two of h16), xscale (per-token power of two)
-  uint32_t* hmax = nullptr;     // [P] float bits of max |h| per bucketed row
+  uint32_t* hmax = nullptr;     // [P] float bits of max |h| (per pick on the decode path, per bucketed
+                                //     row on the GEMM path); zero between calls
   int4* mtiles = nullptr;       // [P/128 + E] {expert, first bucketed row, rows, 0}
   int32_t* nmtiles = nullptr;   // [1]
 };
@@ -163,6 +164,7 @@ struct FfnArgs {
 };
 cudaError_t launch_gateup(const FfnArgs& a, cudaStream_t s);
 cudaError_t launch_down(const FfnArgs& a, cudaStream_t s);
+cudaError_t launch_hconv(const FfnArgs& a, cudaStream_t s);
 cudaError_t launch_combine(const FfnArgs& a, cudaStream_t s);
 // Tensor-core grouped GEMM path (gemm_tc.cu).
 struct GemmFfn {
