@@ -94,6 +94,8 @@ __device__ void logits_and_convert(const RouterArgs& a, uint16_t* xs, float* red
   const int qt = warp % kWarpsPerRow;
   const int nq = a.d / 4, span = nq / kWarpsPerRow, q0 = qt * span, q1 = q0 + span;
   const float4* wr = reinterpret_cast<const float4*>(a.Wr + (size_t)(e < a.E ? e : 0) * a.d);
+  constexpr int kB = 14;  // W_r loads in flight per lane
+  pdl_entry();
   for (int t0 = 0; t0 < a.T; t0 += kTokTile) {
     const int nt = min(kTokTile, a.T - t0);
     __syncthreads();
@@ -103,7 +105,6 @@ __device__ void logits_and_convert(const RouterArgs& a, uint16_t* xs, float* red
       if ((t0 + tt) % (int)gridDim.x == (int)blockIdx.x) convert_token(a, t0 + tt, xs + (size_t)tt * a.d, red);
     float acc[kTokTile] = {0.f, 0.f, 0.f, 0.f};
     if (e < a.E) {
-      constexpr int kB = 14;  // W_r loads in flight per lane
       for (int qb = q0 + lane; qb < q1; qb += 32 * kB) {
         float4 wv[kB];
 #pragma unroll
@@ -493,7 +494,7 @@ __device__ void bucket_small(const int32_t* sidx, const float* sw, int P, int k,
         const int t = m < M ? pk / k : 0;
         U.pick[m] = pk;
         U.tok[m] = t;
-        U.xs[m] = m < M ? __ldcg(xscale + t) : 0.f;
+        U.xs[m] = m < M ? xscale[t] : 0.f;  // shared-memory copy (T <= kUnitTokens)
         U.w[m] = m < M ? sw[pk] : 0.f;
       }
     }
@@ -530,8 +531,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(RouterArgs a)
   __shared__ float red[kRouterWarps];
   __shared__ float part[kRouterWarps * kTokTile];
   __shared__ int last;
-  pdl_entry();
-  logits_and_convert(a, reinterpret_cast<uint16_t*>(rsm), red, part);
+  logits_and_convert(a, reinterpret_cast<uint16_t*>(rsm), red, part);  // (waits on the grid dependency)
   if (!a.fuse_select) return;
   __threadfence();
   __syncthreads();
@@ -547,12 +547,15 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(RouterArgs a)
   int32_t* sidx = reinterpret_cast<int32_t*>(cand + 256);
   float* sw = reinterpret_cast<float*>(sidx + P);
   int* bsm = reinterpret_cast<int*>(sw + P);
+  // token scales for the work units, loaded now so that the top-k hides their latency
+  __shared__ float sxs[kUnitTokens];
+  if (threadIdx.x < min(a.T, kUnitTokens)) sxs[threadIdx.x] = __ldcg(a.ws.xscale + threadIdx.x);
   for (int t = 0; t < a.T; ++t)
     topk_block(a.ws.logits + (size_t)t * a.E, a.bias, a.E, a.k, ku, sg, cand, a.ws.idx + (size_t)t * a.k,
                a.ws.w + (size_t)t * a.k, sidx + (size_t)t * a.k, sw + (size_t)t * a.k);
   if (P <= (int)blockDim.x && a.T <= kUnitTokens)
     bucket_small(sidx, sw, P, a.k, a.E, a.ws.counts, a.ws.offsets, a.ws.perm, a.ws.act, a.ws.nact, a.ws.units,
-                 a.ws.nunits, a.ws.xscale, bsm);
+                 a.ws.nunits, sxs, bsm);
   else
     bucket_block(sidx, P, a.k, a.E, a.ws.counts, a.ws.offsets, a.ws.perm, a.ws.act, a.ws.nact, a.ws.units,
                  a.ws.nunits, sw, a.ws.xscale, bsm, true, true);
