@@ -393,8 +393,6 @@ def run_stack4(args):
         step()
     torch.cuda.synchronize()
     k3.k3moe_cache_reset_stats(cache)
-    for L in layers:
-        k3.k3moe_profile(L, True)
     clocks = ClockSampler(local)
     clocks.start()
     if pg:
@@ -411,6 +409,12 @@ def run_stack4(args):
     ms = e0.elapsed_time(e1)
     clk = clocks.stop()
     st = k3.k3moe_cache_stats(cache)
+    # per-kernel durations: one more step with event pairs around every launch (the events
+    # stop programmatic launch overlap, so the timed steps above run without them)
+    for L in layers:
+        k3.k3moe_profile(L, True)
+    step()
+    torch.cuda.synchronize()
     prof = {}
     for L in layers:
         for kname, (kms, kn) in k3.k3moe_profile_read(L).items():

@@ -154,7 +154,9 @@ int k3moe_bucket(k3moe_layer* layer, const int32_t* idx, int T, int32_t* counts,
  * The result does not depend on the cache budget, on which experts were resident, or on
  * the run (bitwise).  Small T runs the register-decode path, large T the tcgen05 grouped
  * GEMM path (k3moe_set_option); the two agree within the accuracy bound, not bitwise.
- * In cache mode the call synchronises `stream` once (to learn which experts it needs).
+ * In cache mode the call synchronises `stream` once (to learn which experts it needs), unless
+ * every expert of the layer already sits in a slot and the cache has a slot for every expert
+ * of every layer using it (then nothing can be evicted and the lookup is skipped).
  * Errors: INVALID_ARG, CUDA, TIMEOUT, BUDGET_TOO_SMALL, OOM (cache mode). */
 int k3moe_layer_forward(k3moe_layer* layer, const void* x_bf16, int T, float* y, void* stream);
 
@@ -226,6 +228,8 @@ void k3moe_layer_free(k3moe_layer* layer);
  * Least-recently-used experts are replaced; misses are copied from the layer's pinned pool
  * on a side stream.  Errors: INVALID_ARG (budget < one slot), OOM, CUDA. */
 int k3moe_cache_create(size_t budget_bytes, size_t slot_bytes, k3moe_cache** out);
+/* Waits for the layer calls it counts (a device synchronisation when some calls skipped the
+ * lookup: their expert counts are read back asynchronously). */
 int k3moe_cache_stats(const k3moe_cache* cache, k3moe_cache_stats_t* out);
 int k3moe_cache_reset_stats(k3moe_cache* cache);
 /* Destroy after every layer that uses it has been freed or moved to another cache. */

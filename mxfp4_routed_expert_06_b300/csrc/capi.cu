@@ -76,6 +76,14 @@ struct k3moe_cache {
   std::vector<cudaEvent_t> free_events;
   int users = 0;
   int next_uid = 1;
+  long long experts_attached = 0;         // experts of all layers using the cache
+  std::unordered_map<int, int> resident;  // layer uid -> how many of its experts sit in slots
+  // Calls that found every expert of their layer resident with nothing left to evict skip the
+  // host lookup; their active-expert counts are read back asynchronously into this pinned ring
+  // and added to the hit count by k3moe_cache_stats.
+  static constexpr int kRing = 4096;
+  int32_t* ring = nullptr;
+  int ring_n = 0;
 };
 
 struct k3moe_layer {
@@ -178,10 +186,31 @@ int alloc_workspace(k3moe_layer* L) {
   return K3MOE_OK;
 }
 
+// Adds the active-expert counts of the calls that skipped the lookup to the hit count.
+cudaError_t fold_ring(k3moe_cache* C) {
+  if (C->ring_n == 0) return cudaSuccess;
+  const cudaError_t e = cudaDeviceSynchronize();  // the ring's copies ran on the layers' streams
+  if (e != cudaSuccess) return e;
+  for (int i = 0; i < C->ring_n; ++i) C->st.hits += (uint64_t)C->ring[i];
+  C->ring_n = 0;
+  return cudaSuccess;
+}
+
+void attach_cache(k3moe_layer* L, k3moe_cache* C) {
+  L->cache = C;
+  L->uid = C->next_uid++;
+  C->users += 1;
+  C->experts_attached += L->dims.E;
+  C->resident[L->uid] = 0;
+}
+
 // Drops the layer's experts from its cache: their slots become free (least recently used).
 void detach_cache(k3moe_layer* L) {
   k3moe_cache* C = L->cache;
   if (!C) return;
+  fold_ring(C);
+  C->experts_attached -= L->dims.E;
+  C->resident.erase(L->uid);
   for (int s = 0; s < C->n_slots; ++s) {
     if (C->slot_key[s] >= 0 && (int)(C->slot_key[s] >> 32) == L->uid) {
       C->where.erase(C->slot_key[s]);
@@ -270,6 +299,15 @@ int run_routing(k3moe_layer* L, const void* x, int T, cudaStream_t s, bool need_
 int make_resident(k3moe_layer* L, cudaStream_t s) {
   k3moe_cache* C = L->cache;
   const int E = L->dims.E;
+  if ((long long)C->n_slots >= C->experts_attached && C->resident[L->uid] == E) {
+    // every expert of the layer has a slot and nothing can be evicted: the pointer table on
+    // the device is complete, so no lookup (and no host round trip) is needed
+    if (C->ring_n == k3moe_cache::kRing) CUDA_TRY(fold_ring(C));
+    CUDA_TRY(cudaMemcpyAsync(C->ring + C->ring_n, L->ws.nact, 4, cudaMemcpyDeviceToHost, s));
+    C->ring_n += 1;
+    C->st.calls += 1;
+    return K3MOE_OK;
+  }
   CUDA_TRY(cudaMemcpyAsync(L->act_host, L->ws.nact, 4, cudaMemcpyDeviceToHost, s));
   CUDA_TRY(cudaMemcpyAsync(L->act_host + 1, L->ws.act, (size_t)E * 4, cudaMemcpyDeviceToHost, s));
   CUDA_TRY(cudaStreamSynchronize(s));
@@ -308,7 +346,9 @@ int make_resident(k3moe_layer* L, cudaStream_t s) {
       if (C->slot_key[slot] >= 0) {
         C->where.erase(C->slot_key[slot]);
         C->st.evictions += 1;
+        C->resident[(int)(C->slot_key[slot] >> 32)] -= 1;
       }
+      C->resident[L->uid] += 1;
       const long long key = ((long long)L->uid << 32) | e;
       C->slot_key[slot] = key;
       C->where[key] = slot;
@@ -439,6 +479,13 @@ int k3moe_cache_create(size_t budget_bytes, size_t slot_bytes, k3moe_cache** out
     delete C;
     return fail(K3MOE_ERR_CUDA, "cache: stream creation failed");
   }
+  if (cudaHostAlloc((void**)&C->ring, k3moe_cache::kRing * sizeof(int32_t), cudaHostAllocDefault) != cudaSuccess) {
+    cudaGetLastError();
+    cudaStreamDestroy(C->copy_stream);
+    cudaFree(C->slots);
+    delete C;
+    return fail(K3MOE_ERR_OOM, "cache: pinned counter ring allocation failed");
+  }
   C->lru_pos.resize(n);
   C->slot_key.assign(n, -1);
   for (int i = 0; i < (int)n; ++i) {
@@ -452,6 +499,7 @@ int k3moe_cache_create(size_t budget_bytes, size_t slot_bytes, k3moe_cache** out
 int k3moe_cache_stats(const k3moe_cache* cc, k3moe_cache_stats_t* out) {
   if (!cc || !out) return fail(K3MOE_ERR_INVALID_ARG, "NULL argument");
   k3moe_cache* C = const_cast<k3moe_cache*>(cc);
+  CUDA_TRY(fold_ring(C));
   for (auto& pr : C->pending) {
     float ms = 0.f;
     if (cudaEventSynchronize(pr.second) == cudaSuccess && cudaEventElapsedTime(&ms, pr.first, pr.second) == cudaSuccess)
@@ -484,6 +532,7 @@ void k3moe_cache_destroy(k3moe_cache* C) {
   }
   for (auto e : C->free_events) cudaEventDestroy(e);
   cudaFree(C->slots);
+  cudaFreeHost(C->ring);
   delete C;
 }
 
@@ -615,8 +664,7 @@ int k3moe_pack_experts(const k3moe_dims* dims, const void* canon_nib, const void
         cudaSuccess)
       return bail(fail(K3MOE_ERR_CUDA, "pointer table upload failed"));
   } else {
-    L->uid = cache->next_uid++;
-    cache->users += 1;
+    attach_cache(L, cache);
   }
   L->last_stream = s;
   *out = L;
@@ -646,9 +694,7 @@ int k3moe_layer_set_cache(k3moe_layer* L, k3moe_cache* C) {
   if (L->last_stream) CUDA_TRY(cudaStreamSynchronize(L->last_stream));
   if (L->cache) CUDA_TRY(cudaStreamSynchronize(L->cache->copy_stream));
   detach_cache(L);
-  L->cache = C;
-  L->uid = C->next_uid++;
-  C->users += 1;
+  attach_cache(L, C);
   return K3MOE_OK;
 }
 
