@@ -489,8 +489,9 @@ __global__ void __launch_bounds__(128) hconv_kernel(const float* __restrict__ hb
 }
 
 // --------------------------------------------------------------------------- down ---
-// Task = (unit, 16 rows of d) over the whole f range; warp w owns the CTA's tasks j % 8 == w and
-// streams each task in chunks of kc k-tiles (one ring stage per chunk) into a private ring.
+// Task = (unit, 32 rows of d = two 16-row tile groups) over the whole f range; warp w owns the
+// CTA's tasks j % 8 == w and streams each task in chunks of kc k-tiles (one ring stage per chunk:
+// kc tiles of each row group, then the unit's h fragments, which both row groups share).
 constexpr int kDnThreads = kConsumers * 32;
 
 struct DnLayout {
@@ -501,8 +502,8 @@ struct DnLayout {
 inline DnLayout dn_layout(int f, int mcap, size_t budget) {
   DnLayout L;
   const int KT = f / kTileCols;
-  const size_t per_kt = kTileBytes + (size_t)mcap * (4 * 64);  // weights + h fragments
-  int kc = (int)(budget / ((size_t)kConsumers * 3 * per_kt));           // aim for 3 stages per warp
+  const size_t per_kt = 2 * kTileBytes + (size_t)mcap * (4 * 64);  // weights of 2 row groups + h fragments
+  int kc = (int)(budget / ((size_t)kConsumers * 2 * per_kt));           // at least 2 stages per warp
   kc = kc < 1 ? 1 : (kc > KT ? KT : kc);
   L.kc = kc;
   L.nch = (KT + kc - 1) / kc;
@@ -538,13 +539,14 @@ __global__ void __launch_bounds__(kDnThreads, 2) down_kernel(FfnArgs a, DnLayout
   }
   __syncthreads();
 #endif
-  const int RG = a.d / kTileRows;
+  const int RG2 = a.d / (2 * kTileRows);  // tasks per unit: pairs of 16-row groups
   const int KT = a.f / kTileCols;
-  const int ntasks = *a.ws.nunits * RG;
+  const int ntasks = *a.ws.nunits * RG2;
   const size_t gu_bytes = gateup_region_bytes(a.d, a.f);
-  const int wb = L.kc * kTileBytes;  // weight bytes of a full chunk
+  const size_t rg_bytes = (size_t)KT * kTileBytes;  // one row group, all k-tiles
+  const int wb = L.kc * kTileBytes;  // weight bytes of one row group's chunk
   const int G = gridDim.x;
-  // stage: [kc weight tiles][M x kc*256 h fragments]
+  // stage: [kc weight tiles of row group 0][kc of row group 1][M x kc*256 h fragments]
   uint8_t* ring = smem + (size_t)warp * L.depth * L.stage_bytes;
   const uint64_t pol_w = policy_evict_first(), pol_h = policy_evict_normal();
   const int first = blockIdx.x + warp * G, step = kConsumers * G;
@@ -553,28 +555,29 @@ __global__ void __launch_bounds__(kDnThreads, 2) down_kernel(FfnArgs a, DnLayout
 
   int ji = 0, ci = 0;
   DescRegs dcur{0, 0}, dnext{0, 0};
-  const uint8_t* Wcur = nullptr;
+  const uint8_t* Wcur = nullptr;  // row group 0 of the task at the issue cursor (row group 1 follows)
   if (my_tasks > 0) {
-    dcur = load_desc(a.ws.units + first / RG, lane);
-    if (my_tasks > 1) dnext = load_desc(a.ws.units + (first + step) / RG, lane);
-    Wcur = a.expert_ptr[d_e(dcur)] + gu_bytes + (size_t)(first % RG) * KT * kTileBytes;
+    dcur = load_desc(a.ws.units + first / RG2, lane);
+    if (my_tasks > 1) dnext = load_desc(a.ws.units + (first + step) / RG2, lane);
+    Wcur = a.expert_ptr[d_e(dcur)] + gu_bytes + (size_t)(2 * (first % RG2)) * rg_bytes;
   }
   auto issue_next = [&](uint8_t* st) {
     const int kt0 = ci * L.kc, nk = min(L.kc, KT - kt0);
     warp_copy(st, Wcur + (size_t)kt0 * kTileBytes, nk * kTileBytes, lane, pol_w);
+    warp_copy(st + wb, Wcur + rg_bytes + (size_t)kt0 * kTileBytes, nk * kTileBytes, lane, pol_w);
     const int M = d_M(dcur);
     for (int m = 0; m < M; ++m) {
       const int p = d_pick(dcur, m);
-      warp_copy(st + wb + m * L.kc * 256, reinterpret_cast<const uint8_t*>(a.ws.hfrag + (size_t)p * a.f) + kt0 * 256,
-                nk * 256, lane, pol_h);
+      warp_copy(st + 2 * wb + m * L.kc * 256,
+                reinterpret_cast<const uint8_t*>(a.ws.hfrag + (size_t)p * a.f) + kt0 * 256, nk * 256, lane, pol_h);
     }
     if (++ci == L.nch) {
       ci = 0;
       ++ji;
       dcur = dnext;
       if (ji < my_tasks)
-        Wcur = a.expert_ptr[d_e(dcur)] + gu_bytes + (size_t)((first + ji * step) % RG) * KT * kTileBytes;
-      if (ji + 1 < my_tasks) dnext = load_desc(a.ws.units + (first + (ji + 1) * step) / RG, lane);
+        Wcur = a.expert_ptr[d_e(dcur)] + gu_bytes + (size_t)(2 * ((first + ji * step) % RG2)) * rg_bytes;
+      if (ji + 1 < my_tasks) dnext = load_desc(a.ws.units + (first + (ji + 1) * step) / RG2, lane);
     }
   };
   // DEPTH groups always committed ahead (see gateup_kernel)
@@ -589,40 +592,49 @@ __global__ void __launch_bounds__(kDnThreads, 2) down_kernel(FfnArgs a, DnLayout
   }
 
   int rslot = 0;
-  DescRegs dtask = my_tasks > 0 ? load_desc(a.ws.units + first / RG, lane) : DescRegs{0, 0};
+  DescRegs dtask = my_tasks > 0 ? load_desc(a.ws.units + first / RG2, lane) : DescRegs{0, 0};
   for (int j = 0; j < my_tasks; ++j) {
     const int i = first + j * step;
     const DescRegs D = dtask;
-    if (j + 1 < my_tasks) dtask = load_desc(a.ws.units + (i + step) / RG, lane);
+    if (j + 1 < my_tasks) dtask = load_desc(a.ws.units + (i + step) / RG2, lane);
     const int M = d_M(D);
-    const int rg = i % RG;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const int rg = 2 * (i % RG2);
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     for (int c = 0; c < L.nch; ++c) {
       cp_wait<DEPTH - 1>();
       __syncwarp();
       uint8_t* st = ring + (size_t)rslot * L.stage_bytes;
-      const uint8_t* hrow = st + wb + g * L.kc * 256;
+      const uint8_t* hrow = st + 2 * wb + g * L.kc * 256;
       const int nk = min(L.kc, KT - c * L.kc);
       for (int kk = 0; kk < nk; ++kk) {
-        const uint8_t* tp = st + (size_t)kk * kTileBytes;
-        const uint4 u0 = lds128(tp + lane * 16), u1 = lds128(tp + 512 + lane * 16);
-        const uint2 sc = lds64(tp + kTileNibBytes + g * 8);
+        uint4 u[2][2];
+        uint2 sc[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const uint8_t* tp = st + (size_t)r * wb + (size_t)kk * kTileBytes;
+          u[r][0] = lds128(tp + lane * 16);
+          u[r][1] = lds128(tp + 512 + lane * 16);
+          sc[r] = lds64(tp + kTileNibBytes + g * 8);
+        }
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
           const uint4 hv = g < M ? lds128(hrow + (size_t)(4 * kk + b) * 64 + t * 16) : make_uint4(0, 0, 0, 0);
-          const uint4& nv = (b >> 1) ? u1 : u0;
-          float bacc[4];
-          uint32_t A[4];
-          dec4(word_of(nv, 2 * (b & 1)), A);
-          mma_zero(bacc, A, hv.x, hv.y);
-          dec4(word_of(nv, 2 * (b & 1) + 1), A);
-          mma_acc(bacc, A, hv.z, hv.w);
-          const float s_lo = scale_of<ZS>(sc.x, b);
-          const float s_hi = scale_of<ZS>(sc.y, b);
-          acc[0] = fmaf(bacc[0], s_lo, acc[0]);
-          acc[1] = fmaf(bacc[1], s_lo, acc[1]);
-          acc[2] = fmaf(bacc[2], s_hi, acc[2]);
-          acc[3] = fmaf(bacc[3], s_hi, acc[3]);
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const uint4& nv = (b >> 1) ? u[r][1] : u[r][0];
+            float bacc[4];
+            uint32_t A[4];
+            dec4(word_of(nv, 2 * (b & 1)), A);
+            mma_zero(bacc, A, hv.x, hv.y);
+            dec4(word_of(nv, 2 * (b & 1) + 1), A);
+            mma_acc(bacc, A, hv.z, hv.w);
+            const float s_lo = scale_of<ZS>(sc[r].x, b);
+            const float s_hi = scale_of<ZS>(sc[r].y, b);
+            acc[r][0] = fmaf(bacc[0], s_lo, acc[r][0]);
+            acc[r][1] = fmaf(bacc[1], s_lo, acc[r][1]);
+            acc[r][2] = fmaf(bacc[2], s_hi, acc[r][2]);
+            acc[r][3] = fmaf(bacc[3], s_hi, acc[r][3]);
+          }
         }
       }
       __syncwarp();
@@ -640,8 +652,11 @@ __global__ void __launch_bounds__(kDnThreads, 2) down_kernel(FfnArgs a, DnLayout
       const float wp = d_w(D, n);
       if (n < M) {
         const float sc = wp * __ldg(a.ws.hscale + p);  // combine weight x the pick's h scale
-        a.ws.obuf[(size_t)p * a.d + rg * kTileRows + g] = acc[c] * sc;
-        a.ws.obuf[(size_t)p * a.d + rg * kTileRows + g + 8] = acc[2 + c] * sc;
+        float* o = a.ws.obuf + (size_t)p * a.d + (size_t)rg * kTileRows + g;
+        o[0] = acc[0][c] * sc;
+        o[8] = acc[0][2 + c] * sc;
+        o[kTileRows] = acc[1][c] * sc;
+        o[kTileRows + 8] = acc[1][2 + c] * sc;
       }
     }
   }
