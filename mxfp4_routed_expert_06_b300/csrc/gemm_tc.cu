@@ -282,9 +282,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kStages * kStageBytes);
   uint64_t* empty = full + kStages;
-  uint64_t* accf = empty + kStages;  // accumulators ready
-  uint64_t* acce = accf + 1;         // accumulators drained by the epilogue
-  uint64_t* drain = acce + 1;        // final MMA completion
+  uint64_t* accf = empty + kStages;  // [2] accumulators of buffer b ready
+  uint64_t* acce = accf + 2;         // [2] accumulators of buffer b drained by the epilogue
+  uint64_t* drain = acce + 2;        // final MMA completion
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -293,8 +293,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&full[s], MODE == 2 ? 1 : 1 + kDecWarps);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(accf, 1);
-    mbar_init(acce, kEpiWarps);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accf[b], 1);
+      mbar_init(&acce[b], kEpiWarps);
+    }
     mbar_init(drain, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -313,7 +315,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int KS = K / kBK;
   const int KSh = a.d / kBK;
   const int KT = K / kTileCols;
-  const int NT = MODE == 0 ? a.f / 128 : (MODE == 1 ? a.d / a.bn : (a.E + 127) / 128);
+  const int NT = MODE == 0 ? a.f / (a.bn / 2) : (MODE == 1 ? a.d / a.bn : (a.E + 127) / 128);
+  // N <= 128: two accumulator buffers (2 M-tiles x 128 columns each) so that the epilogue of one
+  // item overlaps the next item's MMAs; N = 256: one buffer of 2 x 256 columns
+  const int nbuf = a.bn <= 128 ? 2 : 1;
   const int n_items = (MODE == 2 ? (a.T + 2 * kBM - 1) / (2 * kBM) : *a.nmtiles) * NT;
   const int G = gridDim.x;
   const uint32_t sbase = smem_u32(smem);
@@ -322,7 +327,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ------------------------------------------------------------------ epilogue ---
     int it = 0;
     for (int i = blockIdx.x; i < n_items; i += G, ++it) {
-      if (!wait_phase(accf, (uint32_t)(it & 1), a.err, a.wait_ns)) break;
+      const int buf = it % nbuf, use = it / nbuf;
+      if (!wait_phase(&accf[buf], (uint32_t)(use & 1), a.err, a.wait_ns)) break;
       tc_fence_after();
       const int nt = i % NT;
       const Pair pr = pair_of<MODE>(a, i / NT);
@@ -330,7 +336,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int h = 0; h < 2; ++h) {
         const int rows = h ? pr.rows1 : pr.rows0;
         if (rows <= 0) continue;  // uniform across the warp
-        const uint32_t tb = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(h * 256);
+        const uint32_t tb = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(buf * 256 * (nbuf - 1) + h * a.bn);
         const bool valid = r < rows;
         const int pos = pr.row0 + h * kBM + (valid ? r : 0);
         if (MODE == 2) {
@@ -360,11 +366,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (MODE == 0) {
           const float sc = __ldg(a.ascale + p / a.k) * a.wscale;
           float mx = 0.f;
-          float* dst = a.hbuf + (size_t)pos * a.f + nt * 128;
-          for (int c = 0; c < 4; ++c) {
+          const int half = a.bn / 2;  // gate columns [0, half), up columns [half, bn)
+          float* dst = a.hbuf + (size_t)pos * a.f + nt * half;
+          for (int c = 0; c < half / 32; ++c) {
             uint32_t gr[32], ur[32];
             tmem_ld32(tb + 32 * c, gr);
-            tmem_ld32(tb + 128 + 32 * c, ur);
+            tmem_ld32(tb + half + 32 * c, ur);
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
@@ -401,7 +408,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acce);
+      if (lane == 0) mbar_arrive(&acce[buf]);
     }
   } else if (warp == kMmaWarp) {
     // ----------------------------------------------------------------- MMA issue ---
@@ -412,7 +419,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool ok = true;
       for (int i = blockIdx.x; i < n_items && ok; i += G, ++it) {
         const bool two = pair_of<MODE>(a, i / NT).rows1 > 0;
-        if (!wait_phase(acce, (uint32_t)((it & 1) ^ 1), a.err, a.wait_ns)) break;
+        const int buf = it % nbuf, use = it / nbuf;
+        if (!wait_phase(&acce[buf], (uint32_t)((use & 1) ^ 1), a.err, a.wait_ns)) break;
+        const uint32_t d0 = tmem + (uint32_t)(buf * 256 * (nbuf - 1)), d1 = d0 + (uint32_t)a.bn;
         tc_fence_after();
         for (int ks = 0; ks < KS; ++ks, ++g) {
           const int slot = (int)(g % kStages);
@@ -426,12 +435,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {  // +32 bytes along K per k16 step
             const uint32_t accum = (ks | kk) != 0 ? 1u : 0u;
-            mma_f16(tmem, a0 + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, accum);
-            if (two) mma_f16(tmem + 256u, a1 + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, accum);
+            mma_f16(d0, a0 + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, accum);
+            if (two) mma_f16(d1, a1 + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, accum);
           }
           mma_commit(&empty[slot]);
         }
-        if (ok) mma_commit(accf);
+        if (ok) mma_commit(&accf[buf]);
       }
       // everything issued has completed before TMEM is released
       mma_commit(drain);
@@ -488,9 +497,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int mt = i / NT, nt = i % NT;
       const uint8_t* base = a.expert_ptr[__ldg(&a.mtiles[mt].x)];
       if (MODE == 0) {
-        const int rg = nt * 8 + dw;
-        c_t0 = base + (size_t)rg * KT * 2 * kTileBytes;
-        c_t1 = c_t0 + kTileBytes;
+        if (groups == 16) {  // N = 256: gate rows 16dw.. and up rows 128+16dw.. of row group nt*8+dw
+          c_t0 = base + (size_t)(nt * 8 + dw) * KT * 2 * kTileBytes;
+          c_t1 = c_t0 + kTileBytes;
+        } else {  // N = 128: warps 0-3 take gate row groups nt*4+dw, warps 4-7 the matching up tiles
+          c_t0 = base + (size_t)(nt * 4 + (dw & 3)) * KT * 2 * kTileBytes + (dw >= 4 ? kTileBytes : 0);
+          c_t1 = nullptr;
+        }
       } else {
         c_t0 = base + gu_bytes + (size_t)(nt * groups + dw) * KT * kTileBytes;
         c_t1 = dw + 8 < groups ? c_t0 + (size_t)8 * KT * kTileBytes : nullptr;
@@ -560,9 +573,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           } else {
             const int u = (s % KS) & 1;
             const uint32_t bs = sbase + (uint32_t)(slot * kStageBytes + 2 * kABytes);
-            if (MODE == 0) {
+            if (MODE == 0 && groups == 16) {
               decode(raw[j].n0, raw[j].s0, u, 16 * dw, bs);        // gate rows
               decode(raw[j].n1, raw[j].s1, u, 128 + 16 * dw, bs);  // up rows
+            } else if (MODE == 0) {
+              decode(raw[j].n0, raw[j].s0, u, (dw >= 4 ? 64 : 0) + 16 * (dw & 3), bs);
             } else {
               decode(raw[j].n0, raw[j].s0, u, 16 * dw, bs);
               if (dw + 8 < groups) decode(raw[j].n1, raw[j].s1, u, 16 * (dw + 8), bs);
@@ -762,6 +777,9 @@ GemmArgs common_args(const GemmFfn& q, int mode) {
 
 cudaError_t launch_gemm_gu(const GemmFfn& q, cudaStream_t s) {
   GemmArgs g = common_args(q, 0);
+  // N = 256 (128 gate + 128 up rows per item, one accumulator buffer of 2 x 256 columns):
+  // N = 128 with two buffers overlaps the epilogue but halves the MMA work per decoded
+  // stage, which measured slower (gate/up 3.75 vs 2.78 ms on the K3 prefill)
   g.bn = 256;
   g.ascale = q.xs;
   g.hbuf = q.hbuf;
@@ -778,7 +796,7 @@ cudaError_t launch_gemm_h16(const GemmFfn& q, int P, cudaStream_t s) {
 
 cudaError_t launch_gemm_dn(const GemmFfn& q, cudaStream_t s) {
   GemmArgs g = common_args(q, 1);
-  g.bn = q.d % 256 == 0 ? 256 : 128;
+  g.bn = q.d % 256 == 0 ? 256 : 128;  // N = 256 measured faster than double-buffered N = 128
   g.ascale = q.hs;
   g.obuf = q.obuf;
   CUtensorMap map;
