@@ -288,7 +288,7 @@ int run_routing(k3moe_layer* L, const void* x, int T, cudaStream_t s, bool need_
     if (rc) return rc;
     rc = timed_launch(L, KID_BUCKET, s, [&] {
       return launch_bucket(L->ws.idx, T, D.k, D.E, L->ws.counts, L->ws.offsets, L->ws.perm, L->ws.act, L->ws.nact,
-                           L->ws.units, L->ws.nunits, L->ws.w, L->ws.xscale, s);
+                           L->ws.units, L->ws.nunits, L->ws.w, L->ws.xscale, s, need_frag);
     });
     if (rc) return rc;
   }
@@ -720,7 +720,7 @@ int k3moe_bucket(k3moe_layer* L, const int32_t* idx, int T, int32_t* counts, int
   const k3moe_dims& D = L->dims;
   return timed_launch(L, KID_BUCKET, s, [&] {
     return launch_bucket(idx, T, D.k, D.E, counts, offsets, perm, L->ws.act, L->ws.nact, L->ws.units, L->ws.nunits,
-                         L->ws.w, L->ws.xscale, s);
+                         L->ws.w, L->ws.xscale, s, false);  // the caller gets counts, offsets and perm only
   });
 }
 

@@ -119,7 +119,7 @@ cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, in
                         cudaStream_t s);
 cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* counts, int32_t* offsets,
                           int32_t* perm, int32_t* act, int32_t* nact, UnitDesc* units, int32_t* nunits,
-                          const float* w, const float* xscale, cudaStream_t s);
+                          const float* w, const float* xscale, cudaStream_t s, bool fill_units = true);
 
 // Programmatic dependent launch.  Every kernel of the forward path begins with pdl_entry(): it
 // waits until the previous kernel in the stream has completed and its writes are visible, then

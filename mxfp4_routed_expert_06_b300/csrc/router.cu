@@ -311,9 +311,12 @@ __device__ void topk_block(const float* logits_row, const float* bias, int E, in
 // ------------------------------------------------------------------------ bucketing ---
 // Whole-block deterministic bucketing of P picks.  smem: 2*E ints, plus P ints when
 // perm_smem (small P: the unit descriptors then read perm from shared memory).
+// whist: smem also holds [nwarps][E] per-warp expert counts (zero on entry and on exit), which
+// replaces the warp-by-warp stable scatter with three barriers per block of picks.
 __device__ void bucket_block(const int32_t* idx, int P, int k, int E, int32_t* counts, int32_t* offsets,
                              int32_t* perm, int32_t* act, int32_t* nact, UnitDesc* units, int32_t* nunits,
-                             const float* w, const float* xscale, int* smem, bool perm_smem, bool iw_smem = false) {
+                             const float* w, const float* xscale, int* smem, bool perm_smem, bool iw_smem = false,
+                             int* whist = nullptr, bool fill_units = true) {
   // iw_smem: idx and w are shared-memory arrays of this block (else global, written earlier)
   auto ld_idx = [&](int p) { return iw_smem ? idx[p] : __ldcg(idx + p); };
   auto ld_w = [&](int p) { return iw_smem ? w[p] : __ldcg(w + p); };
@@ -332,8 +335,11 @@ __device__ void bucket_block(const int32_t* idx, int P, int k, int E, int32_t* c
       ev[j] = p < P ? ld_idx(p) : -1;
     }
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (ev[j] >= 0 && ev[j] < E) atomicAdd(&cnt[ev[j]], 1);
+    for (int j = 0; j < 8; ++j) {  // one shared-memory atomic per distinct expert of the warp
+      const int e = (ev[j] >= 0 && ev[j] < E) ? ev[j] : -1;
+      const unsigned same = __match_any_sync(0xffffffffu, e);
+      if (e >= 0 && (same & ((1u << lane) - 1u)) == 0u) atomicAdd(&cnt[e], __popc(same));
+    }
   }
   __syncthreads();
   // block-wide exclusive scan over experts of (picks, active flag, work units); each thread owns
@@ -402,7 +408,7 @@ __device__ void bucket_block(const int32_t* idx, int P, int k, int E, int32_t* c
       counts[e] = v;
       if (v > 0) act[arun++] = e;
       const int np = (v + kUnitTokens - 1) / kUnitTokens;
-      for (int i = 0; i < np; ++i) {
+      for (int i = 0; i < (fill_units ? np : 0); ++i) {
         UnitDesc& U = units[urun + i];
         U.e = e;
         U.M = min(kUnitTokens, v - i * kUnitTokens);
@@ -414,7 +420,31 @@ __device__ void bucket_block(const int32_t* idx, int P, int k, int E, int32_t* c
     }
   }
   __syncthreads();
-  for (int r0 = 0; r0 < P; r0 += bd) {
+  for (int r0 = 0; r0 < P && whist; r0 += bd) {
+    // stable position = running offset of the expert + picks of it in earlier warps of this
+    // block + rank inside the warp
+    const int p = r0 + tid;
+    int e = p < P ? ld_idx(p) : -1;
+    const bool valid = e >= 0 && e < E;
+    if (!valid) e = -1;
+    const unsigned same = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(same & ((1u << lane) - 1u));
+    if (valid && rank == 0) whist[warp * E + e] = __popc(same);
+    __syncthreads();
+    if (valid) {
+      int base = cur[e];
+      for (int w2 = 0; w2 < warp; ++w2) base += whist[w2 * E + e];
+      perm[base + rank] = p;
+      if (perm_smem) sperm[base + rank] = p;
+    }
+    __syncthreads();
+    if (valid && rank == 0) {
+      atomicAdd(&cur[e], __popc(same));
+      whist[warp * E + e] = 0;
+    }
+    __syncthreads();
+  }
+  for (int r0 = 0; r0 < P && !whist; r0 += bd) {
     const int p = r0 + tid;
     int e = p < P ? ld_idx(p) : -1;
     const bool valid = e >= 0 && e < E;
@@ -435,7 +465,8 @@ __device__ void bucket_block(const int32_t* idx, int P, int k, int E, int32_t* c
       __syncthreads();
     }
   }
-  // per-unit pick lists: one thread per (unit, slot m)
+  // per-unit pick lists: one thread per (unit, slot m); only the register-decode FFN reads them
+  if (!fill_units) return;
   __threadfence_block();
   __syncthreads();
   const int nu = s_nunits;
@@ -573,13 +604,21 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* logits,
     topk_block(logits + (size_t)t * E, bias, E, k, ku, sg, cand, idx + (size_t)t * k, w + (size_t)t * k);
 }
 
+constexpr int kWhistMaxE = 1536;  // 34 * E ints of shared memory (<= 204 KB)
+
 __global__ void __launch_bounds__(1024) bucket_kernel(const int32_t* idx, int P, int k, int E, int32_t* counts,
                                                       int32_t* offsets, int32_t* perm, int32_t* act, int32_t* nact,
                                                       UnitDesc* units, int32_t* nunits, const float* w,
-                                                      const float* xscale) {
+                                                      const float* xscale, int fill_units) {
   extern __shared__ int ism[];
   pdl_entry();
-  bucket_block(idx, P, k, E, counts, offsets, perm, act, nact, units, nunits, w, xscale, ism, false);
+  int* whist = nullptr;
+  if (E <= kWhistMaxE) {
+    whist = ism + 2 * E;
+    for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) whist[i] = 0;
+  }
+  bucket_block(idx, P, k, E, counts, offsets, perm, act, nact, units, nunits, w, xscale, ism, false, false, whist,
+               fill_units != 0);
 }
 
 }  // namespace
@@ -611,14 +650,15 @@ cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, in
 
 cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* counts, int32_t* offsets,
                           int32_t* perm, int32_t* act, int32_t* nact, UnitDesc* units, int32_t* nunits,
-                          const float* w, const float* xscale, cudaStream_t s) {
+                          const float* w, const float* xscale, cudaStream_t s, bool fill_units) {
   static bool attr = false;
   if (!attr) {
-    cudaFuncSetAttribute(bucket_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+    cudaFuncSetAttribute(bucket_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 210 * 1024);
     attr = true;
   }
-  return launch_pdl(bucket_kernel, dim3(1), dim3(1024), (size_t)2 * E * sizeof(int), s, idx, T * k, k, E, counts,
-                    offsets, perm, act, nact, units, nunits, w, xscale);
+  const size_t smem = (size_t)(E <= kWhistMaxE ? 34 : 2) * E * sizeof(int);
+  return launch_pdl(bucket_kernel, dim3(1), dim3(1024), smem, s, idx, T * k, k, E, counts, offsets, perm, act,
+                    nact, units, nunits, w, xscale, fill_units ? 1 : 0);
 }
 
 }  // namespace k3
