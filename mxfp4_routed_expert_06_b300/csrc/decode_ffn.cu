@@ -317,6 +317,7 @@ __global__ void __launch_bounds__(kGuThreads, 2) gateup_kernel(FfnArgs a, GuLayo
     int M_n = my_tasks > 0 ? __ldg(&a.ws.units[blockIdx.x / RG].M) : 0;
     for (int j = 0; j < my_tasks; ++j) {
       const int M = M_n;
+      const int gx = g < M ? g : M - 1;
       if (j + 1 < my_tasks) M_n = __ldg(&a.ws.units[(blockIdx.x + (j + 1) * G) / RG].M);
       float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       for (int c = 0; c < cw; ++c) {
@@ -331,10 +332,10 @@ __global__ void __launch_bounds__(kGuThreads, 2) gateup_kernel(FfnArgs a, GuLayo
           nib[m][1] = lds128(st + m * kTileBytes + 512 + lane * 16);
           sc[m] = lds64(st + m * kTileBytes + kTileNibBytes + g * 8);
         }
+        // lanes of absent tokens (g >= M) read token M-1: the MMA columns they feed are not used
         uint4 xv[4];
 #pragma unroll
-        for (int b = 0; b < 4; ++b)
-          xv[b] = g < M ? lds128(st + kGuTileBytes + g * 256 + (b * 4 + t) * 16) : make_uint4(0, 0, 0, 0);
+        for (int b = 0; b < 4; ++b) xv[b] = lds128(st + kGuTileBytes + gx * 256 + (b * 4 + t) * 16);
         __syncwarp();
         if (issued < nstages) {  // refill the slot just read
           issue_next(st);
@@ -604,7 +605,8 @@ __global__ void __launch_bounds__(kDnThreads, 2) down_kernel(FfnArgs a, DnLayout
       cp_wait<DEPTH - 1>();
       __syncwarp();
       uint8_t* st = ring + (size_t)rslot * L.stage_bytes;
-      const uint8_t* hrow = st + 2 * wb + g * L.kc * 256;
+      // lanes of absent picks (g >= M) read pick M-1: the MMA columns they feed are not used
+      const uint8_t* hrow = st + 2 * wb + (g < M ? g : M - 1) * L.kc * 256;
       const int nk = min(L.kc, KT - c * L.kc);
       for (int kk = 0; kk < nk; ++kk) {
         uint4 u[2][2];
@@ -618,7 +620,7 @@ __global__ void __launch_bounds__(kDnThreads, 2) down_kernel(FfnArgs a, DnLayout
         }
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-          const uint4 hv = g < M ? lds128(hrow + (size_t)(4 * kk + b) * 64 + t * 16) : make_uint4(0, 0, 0, 0);
+          const uint4 hv = lds128(hrow + (size_t)(4 * kk + b) * 64 + t * 16);
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
             const uint4& nv = (b >> 1) ? u[r][1] : u[r][0];
