@@ -275,29 +275,44 @@ __global__ void __launch_bounds__(kGuThreads, 2) gateup_kernel(FfnArgs a, GuLayo
     const int my_tasks = blockIdx.x < ntasks ? (ntasks - blockIdx.x + G - 1) / G : 0;
     const long long nstages = (long long)my_tasks * cw;
 
-    // issue cursor: task ji, k-tile index ci; descriptors of task ji and ji+1 (prefetched)
-    int ji = 0, ci = 0;
+    // issue cursor: task ji, k-tile index ci; descriptors of task ji and ji+1 (prefetched).
+    // Wst / x0st: this lane's source bytes of the next stage's weights and of its first token's
+    // x fragments; both advance by a constant stride per stage (k-tiles kt, kt+8, ...).
+    int ji = 0, ci = 0, Mc = 0;
     DescRegs dcur{0, 0}, dnext{0, 0};
-    const uint8_t* Wcur = nullptr;
+    const uint8_t* Wst = nullptr;
+    const uint8_t* x0st = nullptr;
+    const uint8_t* xf = reinterpret_cast<const uint8_t*>(a.ws.xfrag);
+    const size_t xrow = (size_t)a.d * 2;  // bytes of one token's fragments
+    auto enter_task = [&]() {
+      Mc = d_M(dcur);
+      Wst = a.expert_ptr[d_e(dcur)] + (size_t)((blockIdx.x + ji * G) % RG) * gu_stride + (size_t)warp * kGuTileBytes +
+            lane * 16;
+      x0st = xf + (size_t)d_tok(dcur, 0) * xrow + (size_t)warp * 256 + lane * 16;
+    };
     if (my_tasks > 0) {
       dcur = load_desc(a.ws.units + blockIdx.x / RG, lane);
       if (my_tasks > 1) dnext = load_desc(a.ws.units + (blockIdx.x + G) / RG, lane);
-      Wcur = a.expert_ptr[d_e(dcur)] + (size_t)(blockIdx.x % RG) * gu_stride;
+      enter_task();
     }
     auto issue_next = [&](uint8_t* st) {
       // copy the stage at the issue cursor into `st`, then advance the cursor
-      const int kt = warp + kConsumers * ci;
-      warp_copy(st, Wcur + (size_t)kt * kGuTileBytes, kGuTileBytes, lane, pol_w);
-      const int M = d_M(dcur);
-      for (int m = 0; m < M; ++m)
+      uint8_t* dl = st + lane * 16;
+#pragma unroll
+      for (int q = 0; q < kGuTileBytes / 512; ++q) cp16(dl + 512 * q, Wst + 512 * q, pol_w);
+      if (lane * 16 + 512 * (kGuTileBytes / 512) < kGuTileBytes)
+        cp16(dl + 512 * (kGuTileBytes / 512), Wst + 512 * (kGuTileBytes / 512), pol_w);
+      if (lane < 16) cp16(dl + kGuTileBytes, x0st, pol_x);
+      for (int m = 1; m < Mc; ++m)
         warp_copy(st + kGuTileBytes + m * 256,
-                  reinterpret_cast<const uint8_t*>(a.ws.xfrag + (size_t)d_tok(dcur, m) * a.d + (size_t)kt * 128), 256,
-                  lane, pol_x);
+                  xf + (size_t)d_tok(dcur, m) * xrow + (size_t)(warp + kConsumers * ci) * 256, 256, lane, pol_x);
+      Wst += (size_t)kConsumers * kGuTileBytes;
+      x0st += kConsumers * 256;
       if (++ci == cw) {
         ci = 0;
         ++ji;
         dcur = dnext;
-        if (ji < my_tasks) Wcur = a.expert_ptr[d_e(dcur)] + (size_t)((blockIdx.x + ji * G) % RG) * gu_stride;
+        if (ji < my_tasks) enter_task();
         if (ji + 1 < my_tasks) dnext = load_desc(a.ws.units + (blockIdx.x + (ji + 1) * G) / RG, lane);
       }
     };
