@@ -270,7 +270,7 @@ bool use_gemm(const k3moe_layer* L, int T) {
 // it, many tokens take the tensor-core router (logits only).
 int run_routing(k3moe_layer* L, const void* x, int T, cudaStream_t s, bool need_frag) {
   const k3moe_dims& D = L->dims;
-  RouterArgs ra{reinterpret_cast<const uint16_t*>(x), L->Wr, L->bias, T, D.d, D.E, D.k, L->ws, 0};
+  RouterArgs ra{reinterpret_cast<const uint16_t*>(x), L->Wr, L->bias, T, D.d, D.E, D.k, L->ws, 0, need_frag ? 0 : 1};
   // the last router block selects serially token by token: worth it only for a few tokens
   ra.fuse_select = (T <= 4 && T * D.k <= 1024) ? 1 : 0;
   const bool tc = !need_frag && !ra.fuse_select && (long long)T >= L->router_tc_min_t &&

@@ -23,7 +23,7 @@
 //                  max |h| per pick.
 //   hconv_kernel   h -> fp16 B fragments with one power-of-two scale per pick (fp16 never
 //                  overflows; the scale factors out of the down projection's sum).
-//   down_kernel    task = (unit, 16 rows of d) over the whole f range, streamed in chunks of
+//   down_kernel    task = (unit, 32 rows of d) over the whole f range, streamed in chunks of
 //                  k-tiles; consumer warp = task % 8; writes w * hs * o to obuf[pick].
 //   combine_kernel y[t] = sum over the k slots, in slot order, of obuf[t*k + slot].
 // Every device-side wait is bounded (globaltimer); on expiry the kernel sets an error flag
@@ -148,8 +148,9 @@ constexpr int kConsumers = 8;
 constexpr int kStageAlign = 128;
 constexpr int kMaxDepth = 6;  // outstanding cp.async groups per thread
 
-// Asynchronous 16-byte global -> shared copy (L2 only).  The policy argument is unused: the
-// copies go through L2 with the default eviction priority.
+// Asynchronous 16-byte global -> shared copy (L2 only) with an L2 eviction policy: expert bytes
+// are read once per call and go evict-first, so that the router weights and the activations
+// stay in L2 across calls.
 #ifdef K3MOE_DEVICE_CHECKS
 // Self-checking build: a misaligned or out-of-ring copy records kErrBadAccess and is skipped.
 // Bounds are per CTA (shared-window offsets), set by thread 0 before the first copy.
@@ -157,7 +158,6 @@ __shared__ uint32_t g_chk_lo, g_chk_hi;
 __shared__ uint32_t* g_chk_err;
 #endif
 __device__ __forceinline__ void cp16(void* dst, const void* src, uint64_t pol) {
-  (void)pol;
 #ifdef K3MOE_DEVICE_CHECKS
   const uint32_t d = smem_u32(dst);
   if ((d & 15u) != 0u || ((uintptr_t)src & 15u) != 0u || d < g_chk_lo || d + 16u > g_chk_hi) {
@@ -165,7 +165,8 @@ __device__ __forceinline__ void cp16(void* dst, const void* src, uint64_t pol) {
     return;
   }
 #endif
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "l"(pol)
+               : "memory");
 }
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -615,6 +616,17 @@ __global__ void __launch_bounds__(kDnThreads, 2) down_kernel(FfnArgs a, DnLayout
     if (j + 1 < my_tasks) dtask = load_desc(a.ws.units + (i + step) / RG2, lane);
     const int M = d_M(D);
     const int rg = 2 * (i % RG2);
+    // this lane's output columns (picks 2t, 2t+1): pick ids and combine weight x h scale, loaded
+    // now so that the epilogue does not wait on them
+    int pk[2];
+    float osc[2];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int n = 2 * t + c;
+      pk[c] = d_pick(D, n);
+      const float wp = d_w(D, n);
+      osc[c] = n < M ? wp * __ldg(a.ws.hscale + pk[c]) : 0.f;
+    }
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     for (int c = 0; c < L.nch; ++c) {
       cp_wait<DEPTH - 1>();
@@ -664,12 +676,9 @@ __global__ void __launch_bounds__(kDnThreads, 2) down_kernel(FfnArgs a, DnLayout
     }
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
-      const int n = 2 * t + c;
-      const int p = d_pick(D, n);
-      const float wp = d_w(D, n);
-      if (n < M) {
-        const float sc = wp * __ldg(a.ws.hscale + p);  // combine weight x the pick's h scale
-        float* o = a.ws.obuf + (size_t)p * a.d + (size_t)rg * kTileRows + g;
+      if (2 * t + c < M) {
+        const float sc = osc[c];  // combine weight x the pick's h scale
+        float* o = a.ws.obuf + (size_t)pk[c] * a.d + (size_t)rg * kTileRows + g;
         o[0] = acc[0][c] * sc;
         o[8] = acc[0][2 + c] * sc;
         o[kTileRows] = acc[1][c] * sc;

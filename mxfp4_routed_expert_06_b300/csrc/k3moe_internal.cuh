@@ -113,6 +113,7 @@ struct RouterArgs {
   int T, d, E, k;
   Workspace ws;
   int fuse_select;        // 1: last block also does top-k + bucketing (small T)
+  int need_counts;        // 1: the fused bucketing also writes counts / offsets (tensor-core FFN follows)
 };
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* idx, float* w,
@@ -120,6 +121,15 @@ cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, in
 cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* counts, int32_t* offsets,
                           int32_t* perm, int32_t* act, int32_t* nact, UnitDesc* units, int32_t* nunits,
                           const float* w, const float* xscale, cudaStream_t s, bool fill_units = true);
+
+// Atomic add with acquire-release semantics at GPU scope: the caller's earlier writes (and those
+// it observed through a barrier) are visible to whoever reads the new value, and the caller
+// sees the writes that preceded the earlier adds.
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
 
 // Programmatic dependent launch.  Every kernel of the forward path begins with pdl_entry(): it
 // waits until the previous kernel in the stream has completed and its writes are visible, then

@@ -281,16 +281,18 @@ __device__ void topk_block(const float* logits_row, const float* bias, int E, in
     warp_sort<kSortR>(u, id);
     warp_merge32(bu, bi, u[0], id[0]);
   }
+  // pairwise tree of merges: at level h, warp w (w % 2h == 0) merges warp w + h's list into its own
   cand[warp * 32 + lane] = make_uint2(bu, (uint32_t)bi);
-  __syncthreads();
-  if (warp == 0) {
-    uint2 c = cand[lane];
-    uint32_t au = c.x;
-    int ai = (int)c.y;
-    for (int w = 1; w < nw; ++w) {
-      c = cand[w * 32 + lane];
-      warp_merge32(au, ai, c.x, (int)c.y);
+  for (int h = 1; h < nw; h <<= 1) {
+    __syncthreads();
+    if (warp % (2 * h) == 0 && warp + h < nw) {
+      const uint2 c = cand[(warp + h) * 32 + lane];
+      warp_merge32(bu, bi, c.x, (int)c.y);
+      cand[warp * 32 + lane] = make_uint2(bu, (uint32_t)bi);
     }
+  }
+  if (warp == 0) {
+    const int ai = bi;
     const float s = lane < k ? sg[ai] : 0.f;
     float tot = s;
 #pragma unroll
@@ -551,10 +553,88 @@ __device__ void bucket_small(const int32_t* sidx, const float* sw, int P, int k,
   }
 }
 
+// Bucketing of at most 32 picks (T <= kUnitTokens) by one warp: the same stable perm, active
+// list and work units as bucket_small, without the per-expert counts and offsets.  Lane q holds
+// pick q; its rank is the number of picks with a lower expert id, or the same expert and a lower
+// pick id.  A unit starts at each rank whose expert differs from the previous rank's.
+// smem: 2 * 32 ints.  Called by the whole of warp 0.
+__device__ void bucket_warp(const int32_t* sidx, const float* sw, int P, int k, int32_t* perm, int32_t* act,
+                            int32_t* nact, UnitDesc* units, int32_t* nunits, const float* xscale, int* smem) {
+  int* sel = smem;         // [32] expert at rank r
+  int* sperm = smem + 32;  // [32] pick at rank r
+  const int lane = threadIdx.x & 31;
+  const int e = lane < P ? sidx[lane] : 0x7fffffff;
+  int r = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const int ej = __shfl_sync(0xffffffffu, e, j);
+    r += (ej < e) || (ej == e && j < lane);
+  }
+  if (lane < P) {
+    sel[r] = e;
+    sperm[r] = lane;
+  }
+  __syncwarp();
+  const int my = lane < P ? sel[lane] : -1;
+  const int prev = __shfl_up_sync(0xffffffffu, my, 1);
+  const bool start = lane < P && (lane == 0 || prev != my);
+  const unsigned b = __ballot_sync(0xffffffffu, start);
+  if (lane < P) perm[lane] = sperm[lane];
+  if (start) {
+    const int g = __popc(b & ((1u << lane) - 1u));
+    const unsigned after = lane == 31 ? 0u : (b >> (lane + 1));
+    const int M = after ? __ffs(after) : P - lane;  // ranks up to the next start
+    act[g] = my;
+    int pk[kUnitTokens], tk[kUnitTokens];
+    float xv[kUnitTokens], wv[kUnitTokens];
+#pragma unroll
+    for (int m = 0; m < kUnitTokens; ++m) {
+      pk[m] = m < M ? sperm[lane + m] : -1;
+      tk[m] = m < M ? pk[m] / k : 0;
+      xv[m] = m < M ? xscale[tk[m]] : 0.f;
+      wv[m] = m < M ? sw[pk[m]] : 0.f;
+    }
+    int4* U = reinterpret_cast<int4*>(units + g);  // 9 x 16 bytes: header, pick, tok, xs, w
+    U[0] = make_int4(my, M, lane, 0);
+    U[1] = make_int4(pk[0], pk[1], pk[2], pk[3]);
+    U[2] = make_int4(pk[4], pk[5], pk[6], pk[7]);
+    U[3] = make_int4(tk[0], tk[1], tk[2], tk[3]);
+    U[4] = make_int4(tk[4], tk[5], tk[6], tk[7]);
+    float4* Uf = reinterpret_cast<float4*>(U);
+    Uf[5] = make_float4(xv[0], xv[1], xv[2], xv[3]);
+    Uf[6] = make_float4(xv[4], xv[5], xv[6], xv[7]);
+    Uf[7] = make_float4(wv[0], wv[1], wv[2], wv[3]);
+    Uf[8] = make_float4(wv[4], wv[5], wv[6], wv[7]);
+  }
+  if (lane == 0) {
+    *nact = __popc(b);
+    *nunits = __popc(b);
+  }
+}
+
+// counts[e] and offsets[e] (e < E) of picks already in rank order (sel, P entries), whole block
+__device__ void counts_from_sorted(const int* sel, int P, int E, int32_t* counts, int32_t* offsets) {
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int lo = 0, hi = P;  // first rank with expert >= e
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (sel[mid] < e) lo = mid + 1; else hi = mid;
+    }
+    int lo2 = lo, hi2 = P;  // first rank with expert > e
+    while (lo2 < hi2) {
+      const int mid = (lo2 + hi2) >> 1;
+      if (sel[mid] <= e) lo2 = mid + 1; else hi2 = mid;
+    }
+    offsets[e] = lo;
+    counts[e] = lo2 - lo;
+  }
+  if (threadIdx.x == 0) offsets[E] = P;
+}
+
 namespace {
 
 __host__ inline size_t fused_select_smem(int E, int P) {
-  return (size_t)(2 * E + 2) * 4 + 256 * 8 + ((size_t)2 * P + 2 * (size_t)E + P) * 4;
+  return (size_t)(2 * E + 2) * 4 + 256 * 8 + ((size_t)2 * P + std::max<size_t>(2 * (size_t)E + P, 64)) * 4;
 }
 
 __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(RouterArgs a) {
@@ -564,12 +644,12 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(RouterArgs a)
   __shared__ int last;
   logits_and_convert(a, reinterpret_cast<uint16_t*>(rsm), red, part);  // (waits on the grid dependency)
   if (!a.fuse_select) return;
-  __threadfence();
+  // last-block election: the barrier orders the CTA's logit and fragment writes before thread 0's
+  // release; the last CTA's acquire (then its barrier) makes every CTA's writes visible to it
   __syncthreads();
-  if (threadIdx.x == 0) last = (atomicAdd(&a.ws.sync[0], 1u) == gridDim.x - 1);
+  if (threadIdx.x == 0) last = (atom_add_acq_rel(&a.ws.sync[0], 1u) == gridDim.x - 1);
   __syncthreads();
   if (!last) return;
-  __threadfence();
   // shared memory of the last block: [ku: E][sg: E][cand: 256 x 8 bytes][idx: P][w: P][bucketing: 2E + P]
   const int P = a.T * a.k;
   uint32_t* ku = reinterpret_cast<uint32_t*>(rsm);
@@ -584,7 +664,15 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(RouterArgs a)
   for (int t = 0; t < a.T; ++t)
     topk_block(a.ws.logits + (size_t)t * a.E, a.bias, a.E, a.k, ku, sg, cand, a.ws.idx + (size_t)t * a.k,
                a.ws.w + (size_t)t * a.k, sidx + (size_t)t * a.k, sw + (size_t)t * a.k);
-  if (P <= (int)blockDim.x && a.T <= kUnitTokens)
+  if (P <= 32 && a.T <= kUnitTokens) {
+    // few picks: one warp; the per-expert counts only when the tensor-core FFN follows
+    if (threadIdx.x < 32)
+      bucket_warp(sidx, sw, P, a.k, a.ws.perm, a.ws.act, a.ws.nact, a.ws.units, a.ws.nunits, sxs, bsm);
+    if (a.need_counts) {
+      __syncthreads();
+      counts_from_sorted(bsm, P, a.E, a.ws.counts, a.ws.offsets);
+    }
+  } else if (P <= (int)blockDim.x && a.T <= kUnitTokens)
     bucket_small(sidx, sw, P, a.k, a.E, a.ws.counts, a.ws.offsets, a.ws.perm, a.ws.act, a.ws.nact, a.ws.units,
                  a.ws.nunits, sxs, bsm);
   else
