@@ -414,7 +414,7 @@ int forward_gemm(k3moe_layer* L, const void* x, int T, float* y, cudaStream_t s)
   if (rc) return rc;
   rc = timed_launch(L, KID_GEMM_DN, s, [&] { return launch_gemm_dn(q, s); });
   if (rc) return rc;
-  FfnArgs fa{L->eptr_dev, D.d, D.f, D.E, D.k, T, L->ws, y, L->num_sms, L->wait_ns, 0, 0, 0};
+  FfnArgs fa{L->eptr_dev, D.d, D.f, D.E, D.k, T, L->ws, y, L->num_sms, L->wait_ns, 0, 0, 0, nullptr, 0};
   return timed_launch(L, KID_COMBINE, s, [&] { return launch_combine(fa, s); });
 }
 
@@ -435,7 +435,7 @@ int forward_impl(k3moe_layer* L, const void* x, int T, float* y, cudaStream_t s)
     if (rc) return rc;
   }
   FfnArgs fa{L->eptr_dev, D.d, D.f, D.E, D.k, T, L->ws, y, L->num_sms, L->wait_ns, L->test_stall, L->ring_depth,
-             L->zero_scales ? 1 : 0};
+             L->zero_scales ? 1 : 0, L->cache ? nullptr : L->packed, L->exp_bytes};
   L->test_stall = 0;
   rc = timed_launch(L, KID_GATEUP, s, [&] { return launch_gateup(fa, s); });
   if (rc) return rc;

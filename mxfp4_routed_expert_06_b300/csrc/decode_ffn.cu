@@ -178,6 +178,12 @@ __device__ __forceinline__ void warp_copy(uint8_t* dst, const uint8_t* src, int 
   for (int off = lane * 16; off < bytes; off += 512) cp16(dst + off, src + off, pol);
 }
 
+// Packed bytes of expert e: computed from the contiguous pool when there is one, so that a task
+// start waits on one dependent load (its descriptor) instead of two.
+__device__ __forceinline__ const uint8_t* expert_at(const FfnArgs& a, int e) {
+  return a.expert_base ? a.expert_base + (size_t)e * a.expert_stride : a.expert_ptr[e];
+}
+
 // One unit's descriptor spread over a warp: lane l < 36 holds 32-bit word l (lanes 0..31 only
 // hold words 0..31, which cover e, M, pick[8], tok[8], xs[8]; w[8] is words 28..35 and is read
 // through a second register).
@@ -287,7 +293,7 @@ __global__ void __launch_bounds__(kGuThreads, 2) gateup_kernel(FfnArgs a, GuLayo
     const size_t xrow = (size_t)a.d * 2;  // bytes of one token's fragments
     auto enter_task = [&]() {
       Mc = d_M(dcur);
-      Wst = a.expert_ptr[d_e(dcur)] + (size_t)((blockIdx.x + ji * G) % RG) * gu_stride + (size_t)warp * kGuTileBytes +
+      Wst = expert_at(a, d_e(dcur)) + (size_t)((blockIdx.x + ji * G) % RG) * gu_stride + (size_t)warp * kGuTileBytes +
             lane * 16;
       x0st = xf + (size_t)d_tok(dcur, 0) * xrow + (size_t)warp * 256 + lane * 16;
     };
@@ -576,7 +582,7 @@ __global__ void __launch_bounds__(kDnThreads, 2) down_kernel(FfnArgs a, DnLayout
   if (my_tasks > 0) {
     dcur = load_desc(a.ws.units + first / RG2, lane);
     if (my_tasks > 1) dnext = load_desc(a.ws.units + (first + step) / RG2, lane);
-    Wcur = a.expert_ptr[d_e(dcur)] + gu_bytes + (size_t)(2 * (first % RG2)) * rg_bytes;
+    Wcur = expert_at(a, d_e(dcur)) + gu_bytes + (size_t)(2 * (first % RG2)) * rg_bytes;
   }
   auto issue_next = [&](uint8_t* st) {
     const int kt0 = ci * L.kc, nk = min(L.kc, KT - kt0);
@@ -593,7 +599,7 @@ __global__ void __launch_bounds__(kDnThreads, 2) down_kernel(FfnArgs a, DnLayout
       ++ji;
       dcur = dnext;
       if (ji < my_tasks)
-        Wcur = a.expert_ptr[d_e(dcur)] + gu_bytes + (size_t)(2 * ((first + ji * step) % RG2)) * rg_bytes;
+        Wcur = expert_at(a, d_e(dcur)) + gu_bytes + (size_t)(2 * ((first + ji * step) % RG2)) * rg_bytes;
       if (ji + 1 < my_tasks) dnext = load_desc(a.ws.units + (first + (ji + 1) * step) / RG2, lane);
     }
   };

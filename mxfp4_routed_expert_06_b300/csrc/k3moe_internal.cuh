@@ -171,6 +171,8 @@ struct FfnArgs {
   int test_stall;                    // 1: consumers wait on a barrier nothing arrives at (timeout test)
   int ring_depth;                    // 0: automatic; else stages in flight per streaming warp
   int zero_scales;                   // 1: some E8M0 scale byte is 0 (exact subnormal decode needed)
+  const uint8_t* expert_base;        // non-null: expert e is at expert_base + e * expert_stride (no
+  size_t expert_stride;              //   table lookup); null: expert_ptr[e] (device cache mode)
 };
 cudaError_t launch_gateup(const FfnArgs& a, cudaStream_t s);
 cudaError_t launch_down(const FfnArgs& a, cudaStream_t s);
