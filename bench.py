@@ -441,6 +441,32 @@ def run_stack4(args):
             a[0] += kms
             a[1] += kn
         k3.k3moe_profile(L, False)
+    # Cache-policy study: the expert set each call of a step looks up (recorded in an untimed
+    # pass with the library's own top-k on the same layer inputs), replayed as the warm-up and
+    # timed steps through the same number of slots under LRU (the device cache's policy),
+    # Belady's MIN and random replacement; hit rates over the timed steps.
+    slots = budget // EXPERT_BYTES
+    trace = []
+    idx = torch.empty((1, K), dtype=torch.int32, device="cuda")
+    wts = torch.empty((1, K), dtype=torch.float32, device="cuda")
+    for t in range(n_tok):
+        x = xd[t:t + 1]
+        resid.copy_(x)
+        for l, L in enumerate(layers):
+            k3.k3moe_router_topk(L, x, 1, idx, wts, stream)
+            trace.append([l * E + int(e) for e in np.unique(idx.cpu().numpy())])
+            y = ys[t, l:l + 1]
+            k3.k3moe_layer_forward(L, x, 1, y, stream)
+            k3.k3moe_residual_rmsnorm(y, resid, 1, D, 1e-6, resid, xin, stream)
+            x = xin
+    torch.cuda.synchronize()
+    study = {}
+    for name, pol in (("lru", k3.K3MOE_POLICY_LRU), ("min", k3.K3MOE_POLICY_MIN), ("random", k3.K3MOE_POLICY_RANDOM)):
+        warm = k3.k3moe_cache_simulate(trace * args.warmup, slots, pol, SEED)
+        full = k3.k3moe_cache_simulate(trace * (args.warmup + args.steps), slots, pol, SEED)
+        h, m = full["hits"] - warm["hits"], full["misses"] - warm["misses"]
+        study[name] = {"hits": h, "misses": m, "hit_rate": round(h / max(1, h + m), 4)}
+    study["lru_equals_device"] = (study["lru"]["hits"], study["lru"]["misses"]) == (st["hits"], st["misses"])
     value, ms = job_throughput(n_tok * args.steps, ms, pg)
     hbm_peak, _, peak_kind = _peaks()
     gu_ms, gu_n = prof.get("gateup", (0.0, 0))
@@ -461,7 +487,8 @@ def run_stack4(args):
                       "hit_rate": round(st["hits"] / max(1, st["hits"] + st["misses"]), 4),
                       "h2d_gb": round(st["h2d_bytes"] / 1e9, 3),
                       "h2d_gbs_of_copy_time": round(st["h2d_bytes"] / 1e6 / max(st["h2d_ms"], 1e-9), 2),
-                      "h2d_gbs_of_wall": round(st["h2d_bytes"] / 1e6 / ms, 2)},
+                      "h2d_gbs_of_wall": round(st["h2d_bytes"] / 1e6 / ms, 2),
+                      "policy_study": study},
             "roofline": {"bound": "hbm", "kernel": "gateup_kernel (gate/up + SwiGLU, register decode)",
                          "achieved": None if achieved is None else round(achieved, 1), "peak": hbm_peak,
                          "unit": "GB/s", "frac": None if achieved is None else round(achieved / hbm_peak, 4),

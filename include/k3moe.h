@@ -242,6 +242,34 @@ void k3moe_cache_destroy(k3moe_cache* cache);
  * or slot_bytes differ), CUDA. */
 int k3moe_layer_set_cache(k3moe_layer* layer, k3moe_cache* cache);
 
+/* Cache-policy study ("four reductions", expert LRU paragraph, and the hit rates the pages
+ * measure with a cache simulator on a recorded routing trace).  Host only: no device memory,
+ * callable without a GPU.  Replays a trace of layer calls through n_slots expert slots:
+ *   keys        host int64 [call_start[n_calls]]: the experts each call needs resident at once,
+ *               any int64 that names an expert (e.g. layer * E + expert), distinct within a call,
+ *               in the order the call looks them up (the device cache: ascending expert id)
+ *   call_start  host int64 [n_calls + 1], call_start[0] = 0, non-decreasing: call c is
+ *               keys[call_start[c] .. call_start[c+1])
+ *   policy      K3MOE_POLICY_LRU: the device cache's policy (hits touched first, then each miss
+ *               replaces the least recently used slot not touched by the call);
+ *               K3MOE_POLICY_MIN: Belady's offline optimum (a miss in a full cache evicts the
+ *               resident expert the call does not need whose next use is farthest ahead);
+ *               K3MOE_POLICY_RANDOM: a miss in a full cache evicts a uniformly drawn resident
+ *               expert the call does not need (splitmix64 stream seeded by `seed`)
+ * Empty slots fill first (a miss, not an eviction).  out: hits + misses = call_start[n_calls].
+ * Errors: INVALID_ARG (NULL pointers, n_slots < 1, bad call_start, a key repeated within a
+ * call, unknown policy), BUDGET_TOO_SMALL (a call needs more than n_slots experts). */
+#define K3MOE_POLICY_LRU 0
+#define K3MOE_POLICY_MIN 1
+#define K3MOE_POLICY_RANDOM 2
+typedef struct {
+  long long hits;
+  long long misses;
+  long long evictions;
+} k3moe_cache_sim_stats;
+int k3moe_cache_simulate(const int64_t* keys, const int64_t* call_start, int n_calls, int n_slots, int policy,
+                         unsigned long long seed, k3moe_cache_sim_stats* out);
+
 /* Glue between stacked layers (the layer's y excludes any residual).  For T tokens of
  * width d:  x_next = bf16_rne(x + y), the sum in fp32;  x_norm = bf16_rne(x_next /
  * sqrt(mean_j(x_next_j^2) + eps)), a weightless RMSNorm, the input a pre-norm block feeds

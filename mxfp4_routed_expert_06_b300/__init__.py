@@ -51,6 +51,10 @@ class k3moe_cache_stats_t(ctypes.Structure):
                 ("h2d_bytes", ctypes.c_uint64), ("h2d_ms", ctypes.c_double), ("calls", ctypes.c_uint64)]
 
 
+class k3moe_cache_sim_stats(ctypes.Structure):
+    _fields_ = [("hits", ctypes.c_longlong), ("misses", ctypes.c_longlong), ("evictions", ctypes.c_longlong)]
+
+
 class k3moe_kernel_time(ctypes.Structure):
     _fields_ = [("ms_total", ctypes.c_double), ("launches", ctypes.c_longlong)]
 
@@ -76,6 +80,7 @@ _SIGS = {
     "k3moe_cache_destroy": ([_vp], None),
     "k3moe_layer_set_cache": ([_vp, _vp], _i),
     "k3moe_residual_rmsnorm": ([_vp, _vp, _i, _i, ctypes.c_float, _vp, _vp, _vp], _i),
+    "k3moe_cache_simulate": ([_vp, _vp, _i, _i, _i, ctypes.c_ulonglong, ctypes.POINTER(k3moe_cache_sim_stats)], _i),
     "k3moe_last_error": ([], ctypes.c_char_p),
     "k3moe_router_topk_noalloc": ([_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp], _i),
 }
@@ -225,6 +230,20 @@ def k3moe_cache_destroy(cache) -> None:
 
 def k3moe_residual_rmsnorm(y, x, T: int, d: int, eps: float, x_next, x_norm, stream=None) -> None:
     _check(_lib.k3moe_residual_rmsnorm(_ptr(y), _ptr(x), T, d, eps, _ptr(x_next), _ptr(x_norm), _stream(stream)))
+
+
+def k3moe_cache_simulate(calls, n_slots: int, policy: int, seed: int = 0) -> dict:
+    """calls: a sequence of calls, each a sequence of int expert keys (distinct within a call), in
+    the order the call looks them up.  Host only.  Returns {hits, misses, evictions}."""
+    import numpy as np
+    starts = np.zeros(len(calls) + 1, dtype=np.int64)
+    starts[1:] = np.cumsum([len(c) for c in calls])
+    keys = np.ascontiguousarray(np.concatenate([np.asarray(c, dtype=np.int64) for c in calls])
+                                if len(calls) else np.zeros(0, dtype=np.int64))
+    st = k3moe_cache_sim_stats()
+    _check(_lib.k3moe_cache_simulate(keys.ctypes.data, starts.ctypes.data, len(calls), n_slots, policy, seed,
+                                     ctypes.byref(st)))
+    return {n: getattr(st, n) for n, _ in st._fields_}
 
 
 def k3moe_layer_set_cache(layer, cache) -> None:

@@ -14,7 +14,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libk3moe.so")
-SOURCES = ["capi.cu", "pack.cu", "router.cu", "decode_ffn.cu", "noalloc.cu", "glue.cu", "gemm_tc.cu"]
+SOURCES = ["capi.cu", "pack.cu", "router.cu", "decode_ffn.cu", "noalloc.cu", "glue.cu", "gemm_tc.cu", "cachesim.cu"]
 HEADERS = ["k3moe_internal.cuh"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
               "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall", "-Xptxas", "-warn-spills"]

@@ -122,6 +122,10 @@ def test_small_stack_budgets_bit_identical():
         st = k3.k3moe_cache_stats(cache)
         assert st["calls"] == steps * n_layers
         assert st["hits"] + st["misses"] == sum(len(u) for _, u in used)
+        # the host simulator's LRU replays the same trace to the same counts
+        trace = [[l * E + int(e) for e in u] for l, u in used]
+        sim = k3.k3moe_cache_simulate(trace, slots, k3.K3MOE_POLICY_LRU)
+        assert (st["hits"], st["misses"], st["evictions"]) == (sim["hits"], sim["misses"], sim["evictions"])
         assert st["h2d_bytes"] == st["misses"] * eb
         if slots >= n_layers * E:
             assert st["evictions"] == 0 and st["misses"] == total_distinct
@@ -134,6 +138,9 @@ def test_small_stack_budgets_bit_identical():
         st2 = k3.k3moe_cache_stats(cache)
         if slots >= n_layers * E:
             assert st2["misses"] == 0 and st2["hits"] == st["hits"] + st["misses"]
+        sim2 = k3.k3moe_cache_simulate(trace + trace, slots, k3.K3MOE_POLICY_LRU)
+        assert [st2[n] for n in ("hits", "misses", "evictions")] == [sim2[n] - sim[n] for n in
+                                                                     ("hits", "misses", "evictions")]
     for L in cache_layers + dev_layers:
         k3.k3moe_layer_free(L)
     for c in caches:
