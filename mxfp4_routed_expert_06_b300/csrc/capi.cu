@@ -165,8 +165,8 @@ int alloc_workspace(k3moe_layer* L) {
       {(void**)&w.idx, P * 4},           {(void**)&w.w, P * 4},                 {(void**)&w.counts, (size_t)D.E * 4},
       {(void**)&w.offsets, (size_t)(D.E + 1) * 4}, {(void**)&w.perm, P * 4},    {(void**)&w.act, (size_t)D.E * 4},
       {(void**)&w.nact, 4},              {(void**)&w.units, (P / kUnitTokens + D.E + 1) * sizeof(UnitDesc)},
-      {(void**)&w.nunits, 4},            {(void**)&w.hbuf, P * D.f * 4},        {(void**)&w.pair, P * (D.f / 32) * 4},
-      {(void**)&w.hfrag, P * D.f * 2},   {(void**)&w.hscale, P * (D.f / 32) * 4},
+      {(void**)&w.nunits, 4},            {(void**)&w.hbuf, P * D.f * 4},
+      {(void**)&w.hfrag, P * D.f * 2},   {(void**)&w.hscale, P * 4},
       {(void**)&w.obuf, P * D.d * 4},    {(void**)&w.sync, 64},                 {(void**)&w.bad, 16},
       {(void**)&w.hmax, P * 4},          {(void**)&w.mtiles, (P / 128 + D.E + 1) * sizeof(int4)},
       {(void**)&w.nmtiles, 4},
@@ -253,7 +253,6 @@ void free_layer(k3moe_layer* L) {
 cudaError_t reset_after_timeout(k3moe_layer* L) {
   const k3moe_dims& D = L->dims;
   cudaError_t e = cudaMemset(L->ws.sync, 0, 64);
-  if (e == cudaSuccess) e = cudaMemset(L->ws.pair, 0, (size_t)D.T_max * D.k * (D.f / 32) * 4);
   if (e == cudaSuccess) e = cudaMemset(L->ws.hmax, 0, (size_t)D.T_max * D.k * 4);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   return e;

@@ -18,7 +18,7 @@
 // limited by a per-copy cost.
 //   gateup_kernel  task = (unit, 16 rows of f); stage = one 128-column k-tile of the gate and
 //                  up tiles (2176 B) + the unit's x fragments for it; consumer warp w takes
-//                  k-tiles kt % 8 == w; one of 4 epilogue warps adds the 8 partial sums in
+//                  k-tiles kt % 8 == w; one of 2 epilogue warps adds the 8 partial sums in
 //                  warp order, applies SwiGLU h = silu(g) * u, writes h (fp32) and records
 //                  max |h| per pick.
 //   hconv_kernel   h -> fp16 B fragments with one power-of-two scale per pick (fp16 never

@@ -78,9 +78,8 @@ struct Workspace {
   UnitDesc* units = nullptr;    // [P/8 + E] work units
   int32_t* nunits = nullptr;    // [1]
   float* hbuf = nullptr;        // [P][f] SwiGLU output, fp32
-  int32_t* pair = nullptr;      // [P][f/32] (unused since h has one scale per pick; kept zero)
   __half* hfrag = nullptr;      // [P][f] fragment order
-  float* hscale = nullptr;      // [P] power of two per pick (h = hfrag * hscale); sized [P][f/32]
+  float* hscale = nullptr;      // [P] power of two per pick (h = hfrag * hscale)
   float* obuf = nullptr;        // [P][d] w-scaled expert outputs
   uint32_t* sync = nullptr;     // [16]: [0] router last-block ticket, [1] device error flags
   int32_t* bad = nullptr;       // [4] pack time: [0] error flags, [1] min scale byte, [2] max scale byte
