@@ -169,7 +169,7 @@ int alloc_workspace(k3moe_layer* L) {
       {(void**)&w.hfrag, P * D.f * 2},   {(void**)&w.hscale, P * 4},
       {(void**)&w.obuf, P * D.d * 4},    {(void**)&w.sync, 64},                 {(void**)&w.bad, 16},
       {(void**)&w.hmax, P * 4},          {(void**)&w.mtiles, (P / 128 + D.E + 1) * sizeof(int4)},
-      {(void**)&w.nmtiles, 4},
+      {(void**)&w.nmtiles, 4},           {(void**)&w.chist, (P / 2048 + 1) * D.E * 4},
   };
   size_t total = 0;
   for (auto& it : items) total += align256(it.bytes);
@@ -287,7 +287,7 @@ int run_routing(k3moe_layer* L, const void* x, int T, cudaStream_t s, bool need_
     if (rc) return rc;
     rc = timed_launch(L, KID_BUCKET, s, [&] {
       return launch_bucket(L->ws.idx, T, D.k, D.E, L->ws.counts, L->ws.offsets, L->ws.perm, L->ws.act, L->ws.nact,
-                           L->ws.units, L->ws.nunits, L->ws.w, L->ws.xscale, s, need_frag);
+                           L->ws.units, L->ws.nunits, L->ws.w, L->ws.xscale, L->ws.chist, s, need_frag);
     });
     if (rc) return rc;
   }
@@ -719,7 +719,7 @@ int k3moe_bucket(k3moe_layer* L, const int32_t* idx, int T, int32_t* counts, int
   const k3moe_dims& D = L->dims;
   return timed_launch(L, KID_BUCKET, s, [&] {
     return launch_bucket(idx, T, D.k, D.E, counts, offsets, perm, L->ws.act, L->ws.nact, L->ws.units, L->ws.nunits,
-                         L->ws.w, L->ws.xscale, s, false);  // the caller gets counts, offsets and perm only
+                         L->ws.w, L->ws.xscale, L->ws.chist, s, false);  // the caller gets counts, offsets and perm
   });
 }
 

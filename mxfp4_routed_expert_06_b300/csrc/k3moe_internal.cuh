@@ -90,6 +90,7 @@ struct Workspace {
                                 //     row on the GEMM path); zero between calls
   int4* mtiles = nullptr;       // [P/128 + E] {expert, first bucketed row, rows, 0}
   int32_t* nmtiles = nullptr;   // [1]
+  int32_t* chist = nullptr;     // [P/2048 + 1][E] per-chunk expert counts (multi-CTA bucketing)
 };
 
 enum KernelId {
@@ -119,7 +120,8 @@ cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, in
                         cudaStream_t s);
 cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* counts, int32_t* offsets,
                           int32_t* perm, int32_t* act, int32_t* nact, UnitDesc* units, int32_t* nunits,
-                          const float* w, const float* xscale, cudaStream_t s, bool fill_units = true);
+                          const float* w, const float* xscale, int32_t* chist, cudaStream_t s,
+                          bool fill_units = true);
 
 // Atomic add with acquire-release semantics at GPU scope: the caller's earlier writes (and those
 // it observed through a barrier) are visible to whoever reads the new value, and the caller

@@ -709,6 +709,146 @@ __global__ void __launch_bounds__(1024) bucket_kernel(const int32_t* idx, int P,
                fill_units != 0);
 }
 
+// ------------------------------------------------------------- multi-CTA bucketing ---
+// For many picks (the tensor-core path and the bucketing entry point, which need counts,
+// offsets and perm but no unit pick lists): chunk c = picks [c*kBkChunk, (c+1)*kBkChunk).
+//   bucket_hist_kernel     chist[c][e] = picks of expert e in chunk c
+//   bucket_scan_kernel     counts, offsets (exclusive scan over e), active list, unit count;
+//                          chist[c][e] becomes offsets[e] + picks of e in chunks before c
+//   bucket_scatter_kernel  chunk c's picks in pick order: perm[chist[c][e] + rank] = p, the rank
+//                          counting earlier picks of e in the chunk (per-warp histograms)
+// so perm lists every expert's picks in increasing pick id, as the single-block kernel does.
+constexpr int kBkChunk = 2048;
+constexpr int kBkThreads = 1024;
+constexpr int kBkMultiMin = 4096;
+
+__global__ void __launch_bounds__(kBkThreads) bucket_hist_kernel(const int32_t* idx, int P, int E, int32_t* chist) {
+  extern __shared__ int hcnt[];
+  pdl_entry();
+  const int lane = threadIdx.x & 31;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hcnt[e] = 0;
+  __syncthreads();
+  const int p0 = blockIdx.x * kBkChunk;
+  for (int p = p0 + (int)threadIdx.x; p < p0 + kBkChunk; p += blockDim.x) {  // (uniform trip count)
+    int e = p < P ? __ldcg(idx + p) : -1;
+    if (e < 0 || e >= E) e = -1;
+    const unsigned same = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && (same & ((1u << lane) - 1u)) == 0u) atomicAdd(&hcnt[e], __popc(same));
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) chist[(size_t)blockIdx.x * E + e] = hcnt[e];
+}
+
+__global__ void __launch_bounds__(1024) bucket_scan_kernel(int32_t* chist, int C, int E, int32_t* counts,
+                                                           int32_t* offsets, int32_t* act, int32_t* nact,
+                                                           int32_t* nunits) {
+  __shared__ int wsum[3][32];
+  pdl_entry();
+  const int tid = threadIdx.x, bd = blockDim.x, warp = tid >> 5, lane = tid & 31, nwarps = bd >> 5;
+  // each thread owns a contiguous range of experts, so every output stays in expert-id order
+  const int per = (E + bd - 1) / bd;
+  const int ea = min(E, tid * per), eb = min(E, ea + per);
+  int cs = 0, as = 0, us = 0;
+  for (int e = ea; e < eb; ++e) {
+    int v = 0;
+    for (int c = 0; c < C; ++c) v += __ldcg(chist + (size_t)c * E + e);
+    cs += v;
+    as += v > 0;
+    us += (v + kUnitTokens - 1) / kUnitTokens;
+  }
+  int ci = cs, ai = as, ui = us;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int c2 = __shfl_up_sync(0xffffffffu, ci, off), a2 = __shfl_up_sync(0xffffffffu, ai, off),
+              u2 = __shfl_up_sync(0xffffffffu, ui, off);
+    if (lane >= off) {
+      ci += c2;
+      ai += a2;
+      ui += u2;
+    }
+  }
+  if (lane == 31) {
+    wsum[0][warp] = ci;
+    wsum[1][warp] = ai;
+    wsum[2][warp] = ui;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int c0 = lane < nwarps ? wsum[0][lane] : 0, a0 = lane < nwarps ? wsum[1][lane] : 0,
+              u0 = lane < nwarps ? wsum[2][lane] : 0;
+    int cc = c0, aa = a0, uu = u0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int c2 = __shfl_up_sync(0xffffffffu, cc, off), a2 = __shfl_up_sync(0xffffffffu, aa, off),
+                u2 = __shfl_up_sync(0xffffffffu, uu, off);
+      if (lane >= off) {
+        cc += c2;
+        aa += a2;
+        uu += u2;
+      }
+    }
+    __syncwarp();
+    if (lane < nwarps) {
+      wsum[0][lane] = cc - c0;
+      wsum[1][lane] = aa - a0;
+      wsum[2][lane] = uu - u0;
+    }
+    if (lane == 31) {
+      offsets[E] = cc;
+      *nact = aa;
+      *nunits = uu;
+    }
+  }
+  __syncthreads();
+  int run = wsum[0][warp] + ci - cs, arun = wsum[1][warp] + ai - as;
+  for (int e = ea; e < eb; ++e) {
+    const int start = run;
+    for (int c = 0; c < C; ++c) {  // chunk bases in place
+      const size_t at = (size_t)c * E + e;
+      const int v = __ldcg(chist + at);
+      chist[at] = run;
+      run += v;
+    }
+    offsets[e] = start;
+    counts[e] = run - start;
+    if (run > start) act[arun++] = e;
+  }
+}
+
+__global__ void __launch_bounds__(kBkThreads) bucket_scatter_kernel(const int32_t* idx, int P, int E,
+                                                                    const int32_t* chist, int32_t* perm) {
+  extern __shared__ int ssm[];
+  int* cur = ssm;            // [E] next free position of each expert for this chunk
+  int* whist = ssm + E;      // [32][E] picks of each expert in each warp of the current round
+  pdl_entry();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int e = tid; e < E; e += blockDim.x) cur[e] = __ldcg(chist + (size_t)blockIdx.x * E + e);
+  for (int i = tid; i < 32 * E; i += blockDim.x) whist[i] = 0;
+  __syncthreads();
+  const int p0 = blockIdx.x * kBkChunk;
+  for (int r0 = p0; r0 < p0 + kBkChunk; r0 += blockDim.x) {  // (uniform trip count)
+    const int p = r0 + tid;
+    int e = p < P ? __ldcg(idx + p) : -1;
+    const bool valid = e >= 0 && e < E;
+    if (!valid) e = -1;
+    const unsigned same = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(same & ((1u << lane) - 1u));
+    if (valid && rank == 0) whist[warp * E + e] = __popc(same);
+    __syncthreads();
+    if (valid) {
+      int base = cur[e];
+      for (int w2 = 0; w2 < warp; ++w2) base += whist[w2 * E + e];
+      perm[base + rank] = p;
+    }
+    __syncthreads();
+    if (valid && rank == 0) {
+      atomicAdd(&cur[e], __popc(same));
+      whist[warp * E + e] = 0;
+    }
+    __syncthreads();
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s) {
@@ -738,11 +878,25 @@ cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, in
 
 cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* counts, int32_t* offsets,
                           int32_t* perm, int32_t* act, int32_t* nact, UnitDesc* units, int32_t* nunits,
-                          const float* w, const float* xscale, cudaStream_t s, bool fill_units) {
+                          const float* w, const float* xscale, int32_t* chist, cudaStream_t s, bool fill_units) {
   static bool attr = false;
   if (!attr) {
     cudaFuncSetAttribute(bucket_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 210 * 1024);
+    cudaFuncSetAttribute(bucket_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 210 * 1024);
     attr = true;
+  }
+  const int P = T * k;
+  if (!fill_units && chist && P >= kBkMultiMin && E <= kWhistMaxE) {
+    // many picks: histogram, scan and stable scatter spread over chunks of kBkChunk picks
+    const int C = (P + kBkChunk - 1) / kBkChunk;
+    cudaError_t e = launch_pdl(bucket_hist_kernel, dim3(C), dim3(kBkThreads), (size_t)E * sizeof(int), s, idx, P,
+                               E, chist);
+    if (e == cudaSuccess)
+      e = launch_pdl(bucket_scan_kernel, dim3(1), dim3(1024), 0, s, chist, C, E, counts, offsets, act, nact, nunits);
+    if (e == cudaSuccess)
+      e = launch_pdl(bucket_scatter_kernel, dim3(C), dim3(kBkThreads), (size_t)33 * E * sizeof(int), s, idx, P, E,
+                     (const int32_t*)chist, perm);
+    return e;
   }
   const size_t smem = (size_t)(E <= kWhistMaxE ? 34 : 2) * E * sizeof(int);
   return launch_pdl(bucket_kernel, dim3(1), dim3(1024), smem, s, idx, T * k, k, E, counts, offsets, perm, act,
