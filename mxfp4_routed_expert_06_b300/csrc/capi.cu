@@ -265,15 +265,15 @@ bool use_gemm(const k3moe_layer* L, int T) {
 }
 
 // Router + selection + bucketing into the workspace.  need_frag: the register-decode FFN
-// follows, which needs the fp16 fragments of x that the CUDA-core router kernel writes; without
-// it, many tokens take the tensor-core router (logits only).
+// follows, which needs the fp16 fragments of x.  From router_tc_min_t tokens the logits run on
+// the tensor cores (and a small kernel writes the fragments when they are needed); below, the
+// CUDA-core router kernel computes the logits and writes the fragments itself.
 int run_routing(k3moe_layer* L, const void* x, int T, cudaStream_t s, bool need_frag) {
   const k3moe_dims& D = L->dims;
   RouterArgs ra{reinterpret_cast<const uint16_t*>(x), L->Wr, L->bias, T, D.d, D.E, D.k, L->ws, 0, need_frag ? 0 : 1};
   // the last router block selects serially token by token: worth it only for a few tokens
   ra.fuse_select = (T <= 4 && T * D.k <= 1024) ? 1 : 0;
-  const bool tc = !need_frag && !ra.fuse_select && (long long)T >= L->router_tc_min_t &&
-                  (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
+  const bool tc = !ra.fuse_select && (long long)T >= L->router_tc_min_t && (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
   int rc = tc ? timed_launch(L, KID_ROUTER, s,
                              [&] {
                                return launch_router_tc(reinterpret_cast<const uint16_t*>(x), T, D.d, D.E, L->Wsplit,
@@ -281,6 +281,10 @@ int run_routing(k3moe_layer* L, const void* x, int T, cudaStream_t s, bool need_
                              })
               : timed_launch(L, KID_ROUTER, s, [&] { return launch_router(ra, s); });
   if (rc) return rc;
+  if (tc && need_frag) {
+    rc = timed_launch(L, KID_GATHER, s, [&] { return launch_convert(ra, L->num_sms, s); });
+    if (rc) return rc;
+  }
   if (!ra.fuse_select) {
     rc = timed_launch(L, KID_TOPK, s,
                       [&] { return launch_topk(L->ws.logits, L->bias, T, D.E, D.k, L->ws.idx, L->ws.w, s); });

@@ -116,6 +116,7 @@ struct RouterArgs {
   int need_counts;        // 1: the fused bucketing also writes counts / offsets (tensor-core FFN follows)
 };
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
+cudaError_t launch_convert(const RouterArgs& a, int num_sms, cudaStream_t s);  // x -> xfrag, xscale
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* idx, float* w,
                         cudaStream_t s);
 cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* counts, int32_t* offsets,

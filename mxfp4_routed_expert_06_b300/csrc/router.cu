@@ -851,6 +851,26 @@ __global__ void __launch_bounds__(kBkThreads) bucket_scatter_kernel(const int32_
 
 }  // namespace
 
+// x -> fp16 B fragments and the per-token power of two, one CTA per token at a time: the
+// register-decode FFN's input when the logits come from the tensor-core router
+__global__ void __launch_bounds__(kRouterWarps * 32) convert_kernel(RouterArgs a) {
+  extern __shared__ __align__(16) uint8_t csm[];
+  __shared__ float red[kRouterWarps];
+  pdl_entry();
+  uint16_t* xr = reinterpret_cast<uint16_t*>(csm);
+  for (int t = blockIdx.x; t < a.T; t += gridDim.x) {
+    __syncthreads();
+    stage_tokens(a, t, 1, xr);
+    __syncthreads();
+    convert_token(a, t, xr, red);
+  }
+}
+
+cudaError_t launch_convert(const RouterArgs& a, int num_sms, cudaStream_t s) {
+  const int grid = std::min(a.T, 2 * num_sms);
+  return launch_pdl(convert_kernel, dim3(grid), dim3(kRouterWarps * 32), (size_t)a.d * sizeof(uint16_t), s, a);
+}
+
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s) {
   // dynamic shared memory: the staged token tile, reused by the last block for top-k keys
   // (kRouterWarps * E floats) and bucketing (2 * E ints)
