@@ -200,6 +200,28 @@ def test_bucket_entry_point_large():
     L.free()
 
 
+@pytest.mark.parametrize("E,k,T", [
+    (896, 16, 300),    # 4800 picks: chunks of 2048 with a ragged last one (multi-CTA bucketing)
+    (1536, 8, 700),    # the largest E the multi-CTA scatter keeps its per-warp histograms for
+    (2048, 4, 1100),   # larger E: the single-block kernel
+])
+def test_bucket_entry_point_many_picks(E, k, T):
+    L = Small(256, 128, E, k, T)
+    rng = np.random.default_rng(E + T)
+    idx = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    perm = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    for _ in range(2):  # the per-chunk scratch is rewritten each call
+        k3.k3moe_bucket(L.layer, _dev(idx), T, counts, offsets, perm)
+        torch.cuda.synchronize()
+        c_o, o_o, p_o = oracle.bucket(idx, E)
+        assert np.array_equal(counts.cpu().numpy(), c_o)
+        assert np.array_equal(offsets.cpu().numpy(), o_o)
+        assert np.array_equal(perm.cpu().numpy(), p_o)
+    L.free()
+
+
 def test_deterministic_and_host_entry_point():
     L = Small(512, 256, 16, 4, 9)
     x = L.tokens(9)
