@@ -182,6 +182,10 @@ int k3moe_sync(k3moe_layer* layer);
                                    nothing completes until the bound expires (failure-path test) */
 #define K3MOE_OPT_RING_DEPTH 5  /* value 0 (default): automatic; 1..6: stages each streaming warp
                                    keeps in flight (a tuning and test knob; results do not change) */
+#define K3MOE_OPT_TEST_FAIL_COPY 7  /* value n > 0: the n-th cache-miss copy from now reports a
+                                   failure without copying (failure-path test).  That forward returns
+                                   K3MOE_ERR_CUDA; the slot it was filling is forgotten, so later
+                                   calls copy the expert again and their results are unchanged */
 #define K3MOE_PATH_AUTO 0
 #define K3MOE_PATH_DECODE 1
 #define K3MOE_PATH_GEMM 2

@@ -3,6 +3,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <iterator>
 #include <list>
 #include <unordered_map>
 #include <utility>
@@ -116,6 +117,7 @@ struct k3moe_layer {
   int num_sms = 148;
   unsigned long long wait_ns = 2000000000ull;  // bound on device-side waits
   int test_stall = 0;                           // next forward stalls its FFN consumers (timeout test)
+  int test_fail_copy = 0;                       // n > 0: the n-th expert copy from now fails (test)
   int ring_depth = 0;                           // 0: automatic
   bool zero_scales = false;                     // some E8M0 scale byte is 0 (2^-127, a subnormal)
   int s_min = 255, s_max = 0;                   // range of the layer's scale bytes
@@ -358,8 +360,27 @@ int make_resident(k3moe_layer* L, cudaStream_t s) {
       C->lru.push_front(slot);
       C->lru_pos[slot] = C->lru.begin();
       uint8_t* dst = C->slots + (size_t)slot * C->slot_bytes;
-      CUDA_TRY(cudaMemcpyAsync(dst, L->pool + (size_t)e * L->exp_bytes, L->exp_bytes, cudaMemcpyHostToDevice,
-                               C->copy_stream));
+      const bool fake = L->test_fail_copy > 0 && --L->test_fail_copy == 0;  // failure-path test
+      const cudaError_t ce = fake ? cudaErrorInvalidValue
+                                  : cudaMemcpyAsync(dst, L->pool + (size_t)e * L->exp_bytes, L->exp_bytes,
+                                                    cudaMemcpyHostToDevice, C->copy_stream);
+      if (ce != cudaSuccess) {
+        if (!fake) cudaGetLastError();
+        // the slot holds no valid expert: forget it (empty, least recently used) so that no later
+        // call takes it for a hit; the copies issued before it still complete on the copy stream,
+        // and later work on `s` is ordered after them
+        C->where.erase(key);
+        C->slot_key[slot] = -1;
+        C->resident[L->uid] -= 1;
+        C->lru.erase(C->lru_pos[slot]);
+        C->lru.push_back(slot);
+        C->lru_pos[slot] = std::prev(C->lru.end());
+        cudaEventRecord(b, C->copy_stream);
+        C->pending.emplace_back(a, b);
+        cudaStreamWaitEvent(s, b, 0);
+        cudaMemcpyAsync((void*)L->eptr_dev, L->eptr_host, (size_t)E * sizeof(void*), cudaMemcpyHostToDevice, s);
+        return fail(K3MOE_ERR_CUDA, "copying expert %d to its cache slot failed: %s", e, cudaGetErrorString(ce));
+      }
       L->eptr_host[e] = dst;
       C->st.misses += 1;
       C->st.h2d_bytes += L->exp_bytes;
@@ -784,6 +805,10 @@ int k3moe_set_option(k3moe_layer* L, int option, long long value) {
     case K3MOE_OPT_RING_DEPTH:
       if (value < 0 || value > 6) return fail(K3MOE_ERR_INVALID_ARG, "RING_DEPTH must be in 0..6");
       L->ring_depth = (int)value;
+      return K3MOE_OK;
+    case K3MOE_OPT_TEST_FAIL_COPY:
+      if (value < 0 || value > (1LL << 30)) return fail(K3MOE_ERR_INVALID_ARG, "TEST_FAIL_COPY must be in 0..2^30");
+      L->test_fail_copy = (int)value;
       return K3MOE_OK;
     case K3MOE_OPT_TEST_STALL:
       if (value != 0 && value != 1) return fail(K3MOE_ERR_INVALID_ARG, "TEST_STALL must be 0 or 1");

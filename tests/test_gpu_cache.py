@@ -147,6 +147,49 @@ def test_small_stack_budgets_bit_identical():
         k3.k3moe_cache_destroy(c)
 
 
+@pytest.mark.parametrize("fail_at,slots", [(1, 64), (3, 64), (6, 10)])
+def test_failed_expert_copy_reports_error_then_recovers(fail_at, slots):
+    """A cache-miss copy that fails (injected on the host: the copy call reports an error and
+    copies nothing) makes that forward return K3MOE_ERR_CUDA; the slot it was filling is
+    forgotten, so the following calls copy the expert again and give the device-resident
+    output, byte for byte."""
+    d, f, E, k, T, steps = 512, 256, 32, 4, 2, 6
+    dm = k3.dims(d, f, E, k, T)
+    eb = k3.k3moe_packed_expert_bytes(dm)
+    nib, scl = synth.experts(9, 0, 0, E, d, f)
+    Wr = synth.router_weights(9, 0, E, d)
+    xs = [torch.from_numpy(synth.tokens_bf16(9, 0, s * T, T, d).view(np.int16)).cuda() for s in range(steps)]
+    ref_layer = k3.k3moe_pack_experts(dm, nib, scl, 0, Wr)
+    cache = k3.k3moe_cache_create(slots * eb, eb)
+    layer = k3.k3moe_pack_experts(dm, nib, scl, 0, Wr, None, cache)
+    try:
+        refs = []
+        for x in xs:
+            y = torch.empty((T, d), dtype=torch.float32, device="cuda")
+            k3.k3moe_layer_forward(ref_layer, x, T, y)
+            refs.append(y)
+        torch.cuda.synchronize()
+        k3.k3moe_set_option(layer, k3.K3MOE_OPT_TEST_FAIL_COPY, fail_at)
+        y = torch.empty((T, d), dtype=torch.float32, device="cuda")
+        with pytest.raises(k3.K3MoEError) as ei:
+            for x in xs:  # the failure comes on the fail_at-th miss, in whichever call makes it
+                k3.k3moe_layer_forward(layer, x, T, y)
+                torch.cuda.synchronize()
+        assert ei.value.code == k3.K3MOE_ERR_CUDA and "cache slot" in str(ei.value)
+        for _ in range(2):  # every later call is whole again, cold slots or warm
+            for x, r in zip(xs, refs):
+                y = torch.empty((T, d), dtype=torch.float32, device="cuda")
+                k3.k3moe_layer_forward(layer, x, T, y)
+                torch.cuda.synchronize()
+                assert torch.equal(y, r)
+        st = k3.k3moe_cache_stats(cache)
+        assert st["h2d_bytes"] == st["misses"] * eb
+    finally:
+        k3.k3moe_layer_free(layer)
+        k3.k3moe_layer_free(ref_layer)
+        k3.k3moe_cache_destroy(cache)
+
+
 def test_budget_too_small_then_recovers():
     d, f, E, k, T = 256, 128, 16, 4, 2
     dm = k3.dims(d, f, E, k, T)
