@@ -122,6 +122,9 @@ def test_tiny_config_c1():
     (1024, 512, 64, 6, 64),
     (384, 128, 12, 3, 129),
     (512, 256, 40, 9, 120),   # 1080 picks: separate top-k and bucketing kernels
+    (256, 128, 64, 32, 1),    # 32 picks (k = 32): the one-warp fused bucketing at its limit
+    (256, 256, 24, 16, 2),    # 32 picks (k = 16, T = 2)
+    (256, 128, 48, 11, 3),    # 33 picks: the block-wide fused bucketing
 ])
 def test_small_configs(d, f, E, k, T):
     L = Small(d, f, E, k, T, seed=d + f + E + k + T)
