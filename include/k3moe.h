@@ -115,8 +115,13 @@ int k3moe_router_topk(k3moe_layer* layer, const void* x_bf16, int T, int32_t* id
  * have no counterpart: this entry point exists for callers that cannot call cudaMalloc --
  * code running inside a host framework whose memory pool already owns the device memory
  * (another allocation may fail or bypass the framework's accounting), or loops where an
- * allocation's implicit device synchronisation is not acceptable.  It computes exactly what
- * k3moe_router_topk computes (same kernels' arithmetic, bitwise the same idx and w), from
+ * allocation's implicit device synchronisation is not acceptable.  It applies the same routing
+ * rule as k3moe_router_topk, with the same ranking (descending sigma + bias, ties to the lower
+ * expert id, NaN and infinite keys ordered by their bits, every id in 0..E-1), but its fp32
+ * logits come from its own GEMV, whose summation order differs from k3moe_router_topk's (and
+ * from 64 tokens on, k3moe_router_topk computes the logits on the tensor cores from W_r split
+ * into bf16 hi + lo, within 4e-4 of fp32).  So: idx equals k3moe_router_topk's on every token
+ * whose k-th and (k+1)-th keys differ by at least 1e-3, and w agrees within 1e-5.  It reads
  * caller buffers:
  *   x     device, [T][d] bf16 (8-byte aligned);  W_r device, [E][d] float32 (16-byte aligned)
  *   bias  device, [E] float32, or NULL;  idx device, [T][k] int32;  w device, [T][k] float32

@@ -35,10 +35,17 @@ int fail(int code, const char* msg) {
 
 __device__ __forceinline__ float sig(float z) { return 1.0f / (1.0f + expf(-z)); }
 
+// A float's bits as an unsigned integer with the same order (larger float -> larger integer);
+// NaNs land at the two ends according to their sign bit.
+__device__ __forceinline__ uint32_t ord_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 __global__ void __launch_bounds__(kWarps * 32) router_topk_noalloc_kernel(
     const uint16_t* __restrict__ x, const float* __restrict__ Wr, const float* __restrict__ bias, int T, int d, int E,
     int k, int32_t* __restrict__ idx, float* __restrict__ w, unsigned char* scratch) {
-  extern __shared__ float keys[];
+  extern __shared__ unsigned long long keys[];  // [kWarps][E] rank keys of the last block
   __shared__ int last;
   unsigned int* ticket = reinterpret_cast<unsigned int*>(scratch);
   float* logits = reinterpret_cast<float*>(scratch + kTicketBytes);
@@ -77,7 +84,14 @@ __global__ void __launch_bounds__(kWarps * 32) router_topk_noalloc_kernel(
   __syncthreads();
   if (!last) return;
   __threadfence();
-  float* ks = keys + (size_t)warp * E;
+  // Top-k per token, one warp per token.  Every expert j gets the 64-bit rank key
+  //   (order-preserving bits of sigma + bias) << 32  |  ~j
+  // so a larger rank key means a larger selection key, or an equal one and a lower expert id:
+  // the same total order as k3moe_router_topk, NaN and infinite keys included.  Every real
+  // entry's rank key is nonzero (its low word ~j is), and a picked entry is set to 0, so the
+  // warp-wide maximum of each of the k rounds is always an entry not yet picked: every selected
+  // id lies in 0..E-1 whatever the key values (E >= k is checked on the host).
+  unsigned long long* ks = keys + (size_t)warp * E;
   for (int t = warp; t < T; t += kWarps) {
     const float* row = logits + (size_t)t * E;
     for (int j0 = 0; j0 < E; j0 += 32 * 16) {  // 16 loads in flight per lane
@@ -91,30 +105,30 @@ __global__ void __launch_bounds__(kWarps * 32) router_topk_noalloc_kernel(
 #pragma unroll
       for (int q = 0; q < 16; ++q) {
         const int j = j0 + 32 * q + lane;
-        if (j < E) ks[j] = sig(z[q]) + bb[q];
+        if (j < E) ks[j] = ((unsigned long long)ord_key(sig(z[q]) + bb[q]) << 32) | (unsigned long long)(~(uint32_t)j);
       }
     }
     __syncwarp();
     int mine = -1;
     for (int i = 0; i < k; ++i) {
-      float bk = -INFINITY;
-      int bi = 0x7fffffff;
+      unsigned long long best = 0ull;
       for (int j = lane; j < E; j += 32) {
-        const float v = ks[j];
-        if (v > bk || (v == bk && j < bi)) { bk = v; bi = j; }
+        const unsigned long long c = ks[j];
+        best = c > best ? c : best;
       }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
-        const float ok = __shfl_xor_sync(0xffffffffu, bk, off);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-        if (ok > bk || (ok == bk && oi < bi)) { bk = ok; bi = oi; }
+        const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
+        best = o > best ? o : best;
       }
+      const int bi = (int)(~(uint32_t)(best & 0xffffffffull));
       if (lane == i) mine = bi;
       __syncwarp();
-      if (lane == 0 && bi < E) ks[bi] = -INFINITY;
+      if (lane == 0 && best != 0ull && bi >= 0 && bi < E) ks[bi] = 0ull;
       __syncwarp();
     }
-    const float s = (lane < k && mine >= 0) ? sig(__ldcg(row + mine)) : 0.f;
+    const bool ok = lane < k && mine >= 0 && mine < E;
+    const float s = ok ? sig(__ldcg(row + mine)) : 0.f;
     float tot = s;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
@@ -146,7 +160,7 @@ int scratch_for_current_device(unsigned char** out) {
     if (e != cudaSuccess || p == nullptr)
       return fail(K3MOE_ERR_CUDA, (std::string("cudaGetSymbolAddress(no-alloc scratch): ") + cudaGetErrorString(e)).c_str());
     cudaError_t a = cudaFuncSetAttribute(router_topk_noalloc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kWarps * 4096 * (int)sizeof(float));
+                                         kWarps * 4096 * (int)sizeof(unsigned long long));
     if (a != cudaSuccess) return fail(K3MOE_ERR_CUDA, (std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(a)).c_str());
     g_dev[dev].ptr = p;
     g_dev[dev].ready = true;
@@ -175,7 +189,7 @@ extern "C" int k3moe_router_topk_noalloc(const void* x_bf16, const float* W_r, c
   if (cudaMemsetAsync(scratch, 0, sizeof(unsigned int), s) != cudaSuccess)
     return fail(K3MOE_ERR_CUDA, "clearing the no-alloc ticket failed");
   const int grid = (E + kWarps - 1) / kWarps;
-  router_topk_noalloc_kernel<<<grid, kWarps * 32, (size_t)kWarps * E * sizeof(float), s>>>(
+  router_topk_noalloc_kernel<<<grid, kWarps * 32, (size_t)kWarps * E * sizeof(unsigned long long), s>>>(
       reinterpret_cast<const uint16_t*>(x_bf16), W_r, bias, T, d, E, k, idx, w, scratch);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(K3MOE_ERR_CUDA, (std::string("router_topk_noalloc launch: ") + cudaGetErrorString(e)).c_str());
