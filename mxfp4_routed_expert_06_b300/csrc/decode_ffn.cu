@@ -746,25 +746,17 @@ int pick_depth(Layout& L, int requested) {
 
 template <int DEPTH, bool ZS>
 cudaError_t launch_gu(const FfnArgs& a, const GuLayout& L, cudaStream_t s) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e =
-        cudaFuncSetAttribute(gateup_kernel<DEPTH, ZS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<unsigned long long> attr{0};
+  const cudaError_t e = set_smem_limit_once(gateup_kernel<DEPTH, ZS>, (int)kSmemBudget, attr);
+  if (e != cudaSuccess) return e;
   return launch_pdl(gateup_kernel<DEPTH, ZS>, dim3(a.num_sms * kCtasPerSm), dim3(kGuThreads), L.total, s, a, L);
 }
 
 template <int DEPTH, bool ZS>
 cudaError_t launch_dn(const FfnArgs& a, const DnLayout& L, cudaStream_t s) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e =
-        cudaFuncSetAttribute(down_kernel<DEPTH, ZS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<unsigned long long> attr{0};
+  const cudaError_t e = set_smem_limit_once(down_kernel<DEPTH, ZS>, (int)kSmemBudget, attr);
+  if (e != cudaSuccess) return e;
   return launch_pdl(down_kernel<DEPTH, ZS>, dim3(a.num_sms * kCtasPerSm), dim3(kDnThreads), L.total, s, a, L);
 }
 

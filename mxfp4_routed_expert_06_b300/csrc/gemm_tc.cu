@@ -730,12 +730,9 @@ cudaError_t activation_map(CUtensorMap* m, const void* base, int K, int rows,
 template <int MODE>
 cudaError_t launch_gemm_mode(const CUtensorMap& map, const CUtensorMap& map_b, const GemmArgs& g, int grid,
                              cudaStream_t s) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<unsigned long long> attr{0};
+  const cudaError_t e = set_smem_limit_once(gemm_kernel<MODE>, (int)kGemmSmem, attr);
+  if (e != cudaSuccess) return e;
   return launch_pdl(gemm_kernel<MODE>, dim3(grid), dim3(kGemmThreads), kGemmSmem, s, map, map_b, g);
 }
 

@@ -1,6 +1,7 @@
 // k3moe_internal.cuh -- shared definitions of the CUDA path (not part of the C ABI).
 #pragma once
 
+#include <atomic>
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <cstddef>
@@ -157,6 +158,22 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   cfg.numAttrs = 1;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
   return e == cudaSuccess ? cudaGetLastError() : e;
+}
+
+// Raises a kernel's dynamic shared-memory limit on the current device.  The attribute belongs
+// to the device, so each call site keeps one bit per device (devices 0..63) and sets it the
+// first time that device launches the kernel; a process that drives several GPUs sets it on
+// each of them.  Devices beyond 63 set it on every call.
+template <typename Fn>
+inline cudaError_t set_smem_limit_once(Fn* kernel, int bytes, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit != 0ull && (done.load(std::memory_order_acquire) & bit) != 0ull) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit != 0ull) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
 }
 
 // Device error flags (ws.sync[1]).

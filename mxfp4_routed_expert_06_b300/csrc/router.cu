@@ -876,22 +876,18 @@ cudaError_t launch_router(const RouterArgs& a, cudaStream_t s) {
   // (kRouterWarps * E floats) and bucketing (2 * E ints)
   size_t smem = (size_t)std::min(a.T, kTokTile) * a.d * sizeof(uint16_t);
   if (a.fuse_select) smem = std::max(smem, fused_select_smem(a.E, a.T * a.k));
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    attr = true;
-  }
+  static std::atomic<unsigned long long> attr{0};
+  const cudaError_t e = set_smem_limit_once(router_kernel, 200 * 1024, attr);
+  if (e != cudaSuccess) return e;
   const int grid = (a.E + kRowsPerCta - 1) / kRowsPerCta;
   return launch_pdl(router_kernel, dim3(grid), dim3(kRouterWarps * 32), smem, s, a);
 }
 
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* idx, float* w,
                         cudaStream_t s) {
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    attr = true;
-  }
+  static std::atomic<unsigned long long> attr{0};
+  const cudaError_t e = set_smem_limit_once(topk_kernel, 200 * 1024, attr);
+  if (e != cudaSuccess) return e;
   const size_t smem = (size_t)(2 * E + 2) * 4 + 256 * 8;
   return launch_pdl(topk_kernel, dim3(std::min(T, 148 * 8)), dim3(kTopkThreads), smem, s, logits, bias, T, E, k, idx, w);
 }
@@ -899,17 +895,15 @@ cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, in
 cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* counts, int32_t* offsets,
                           int32_t* perm, int32_t* act, int32_t* nact, UnitDesc* units, int32_t* nunits,
                           const float* w, const float* xscale, int32_t* chist, cudaStream_t s, bool fill_units) {
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(bucket_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 210 * 1024);
-    cudaFuncSetAttribute(bucket_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 210 * 1024);
-    attr = true;
-  }
+  static std::atomic<unsigned long long> attr_b{0}, attr_s{0};
+  cudaError_t e = set_smem_limit_once(bucket_kernel, 210 * 1024, attr_b);
+  if (e == cudaSuccess) e = set_smem_limit_once(bucket_scatter_kernel, 210 * 1024, attr_s);
+  if (e != cudaSuccess) return e;
   const int P = T * k;
   if (!fill_units && chist && P >= kBkMultiMin && E <= kWhistMaxE) {
     // many picks: histogram, scan and stable scatter spread over chunks of kBkChunk picks
     const int C = (P + kBkChunk - 1) / kBkChunk;
-    cudaError_t e = launch_pdl(bucket_hist_kernel, dim3(C), dim3(kBkThreads), (size_t)E * sizeof(int), s, idx, P,
+    e = launch_pdl(bucket_hist_kernel, dim3(C), dim3(kBkThreads), (size_t)E * sizeof(int), s, idx, P,
                                E, chist);
     if (e == cudaSuccess)
       e = launch_pdl(bucket_scan_kernel, dim3(1), dim3(1024), 0, s, chist, C, E, counts, offsets, act, nact, nunits);
