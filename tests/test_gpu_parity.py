@@ -311,10 +311,9 @@ def test_k3_batched_decode_t64(k3_layer):
     c_o, o_o, p_o = oracle.bucket(idx, K3E)
     assert np.array_equal(counts.cpu().numpy(), c_o) and np.array_equal(perm.cpu().numpy(), p_o)
     assert np.array_equal(offsets.cpu().numpy(), o_o)
-    # y on sampled tokens: first, last and one in between
-    for t in (0, 37, T - 1):
-        y_o, sa = _k3_oracle_y(x[t:t + 1], i_o[t:t + 1], w_o[t:t + 1])
-        assert_y_close(y[t:t + 1], y_o, sa, f"K3 T=64 token {t}")
+    # y on every token of the batch, element by element
+    y_o, sa = _k3_oracle_y(x, i_o, w_o)
+    assert_y_close(y, y_o, sa, "K3 T=64, all tokens")
     # whole-batch invariant at any size: bitwise repeatable
     _, _, y2 = _run(layer, x)
     assert np.array_equal(y, y2)

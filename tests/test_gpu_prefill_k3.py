@@ -1,0 +1,109 @@
+"""The Kimi K3 prefill workload at its own size, through the C ABI, against the fp64 oracle.
+
+One K3-shaped layer (d=7168, f=1536, E=896, k=16) with T=4096 tokens and a +2.0 selection bias on
+32 seeded experts: the benchmark's prefill configuration.  The bias is added after the sigmoid and
+steers only the selection ("kimi-k3-in-c deep dive", invariants table, row 5), so every token's
+top-16 lies among the 32 hot experts and each of them gets about 2048 picks -- 16 M-tiles, i.e.
+eight two-M-tile work items of the tensor-core GEMM per expert, and 65,536 picks for the
+multi-CTA bucketing.  The AUTO path takes the tcgen05 grouped GEMM here.
+
+Checked:
+  * routing: exact top-k sets (and slot order wherever the oracle keys are separated) on all
+    4096 gap-filtered tokens, weights within 1e-5;
+  * bucketing: counts, offsets and perm of all 65,536 picks bit-exact;
+  * y within 2e-3 * sum|terms| + 1e-5 per element on a seeded sample of 64 tokens plus the first
+    and the last, each against the oracle's own routing;
+  * bitwise repeatability of the whole batch.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import assert_routing_matches, assert_y_close, gap_filtered_tokens
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import mxfp4_routed_expert_06_b300 as k3  # noqa: E402
+
+D, F, E, K, T = 7168, 1536, 896, 16, 4096
+SEED = 2026          # the benchmark's seed: the same experts, router and hot subset
+N_HOT = 32
+
+
+def _dev(a):
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(a).cuda()
+
+
+def test_k3_prefill_t4096_hot_experts():
+    nb, sb = synth.expert_bytes(D, F)
+    dn = torch.empty(E * nb, dtype=torch.uint8, device="cuda")
+    ds = torch.empty(E * sb, dtype=torch.uint8, device="cuda")
+    synth.experts_to_device(SEED, 0, 0, E, D, F, dn.data_ptr(), ds.data_ptr())
+    Wr = synth.router_weights(SEED, 0, E, D)
+    bias = synth.hot_bias(SEED, 0, E, N_HOT, 2.0)
+    hot = set(np.nonzero(bias)[0].tolist())
+    L = k3.k3moe_pack_experts(k3.dims(D, F, E, K, T), dn, ds, 1, _dev(Wr), _dev(bias))
+    del dn, ds
+    torch.cuda.empty_cache()
+    try:
+        x, _ = gap_filtered_tokens(SEED, 0, 0, T, D, Wr, bias, K)
+        i_o, w_o, _, keys_o = oracle.router(x, Wr, bias, K)
+        xd = _dev(x)
+
+        # routing on all tokens
+        idx = torch.empty((T, K), dtype=torch.int32, device="cuda")
+        w = torch.empty((T, K), dtype=torch.float32, device="cuda")
+        k3.k3moe_router_topk(L, xd, T, idx, w)
+        torch.cuda.synchronize()
+        idx_h, w_h = idx.cpu().numpy(), w.cpu().numpy()
+        assert set(np.unique(idx_h).tolist()) <= hot
+        assert_routing_matches(idx_h, w_h, i_o, w_o, keys_o)
+
+        # bucketing of all 65,536 picks
+        counts = torch.empty(E, dtype=torch.int32, device="cuda")
+        offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+        perm = torch.empty(T * K, dtype=torch.int32, device="cuda")
+        k3.k3moe_bucket(L, idx, T, counts, offsets, perm)
+        torch.cuda.synchronize()
+        c_o, o_o, p_o = oracle.bucket(idx_h, E)
+        assert np.array_equal(counts.cpu().numpy(), c_o)
+        assert np.array_equal(offsets.cpu().numpy(), o_o)
+        assert np.array_equal(perm.cpu().numpy(), p_o)
+        assert c_o.max() > 7 * 256, "hot experts should span more than one two-M-tile work item"
+
+        # the whole layer on the AUTO path, which must be the tensor-core GEMM at this size
+        k3.k3moe_profile(L, 1)
+        y = torch.empty((T, D), dtype=torch.float32, device="cuda")
+        k3.k3moe_layer_forward(L, xd, T, y)
+        k3.k3moe_sync(L)
+        prof = k3.k3moe_profile_read(L)
+        k3.k3moe_profile(L, 0)
+        assert prof["gemm_gu"][1] == 1 and prof["gemm_dn"][1] == 1 and prof["gateup"][1] == 0
+        y_h = y.cpu().numpy()
+        assert np.isfinite(y_h).all()
+
+        rng = np.random.default_rng(SEED)
+        sample = sorted(set(rng.choice(np.arange(1, T - 1), size=64, replace=False).tolist()) | {0, T - 1})
+        cache = {}
+        nibs, scls = [], []
+        for t in sample:
+            for e in i_o[t].tolist():
+                if e not in cache:
+                    n_, s_ = synth.experts(SEED, 0, e, e + 1, D, F)
+                    cache[e] = (n_[0], s_[0])
+                nibs.append(cache[e][0])
+                scls.append(cache[e][1])
+        y_o, sumabs = oracle.moe(x[sample], w_o[sample], nibs, scls, F)
+        assert_y_close(y_h[sample], y_o, sumabs, f"K3 prefill T={T}, {len(sample)} sampled tokens")
+
+        y2 = torch.empty_like(y)
+        k3.k3moe_layer_forward(L, xd, T, y2)
+        k3.k3moe_sync(L)
+        assert torch.equal(y, y2), "prefill output not bitwise repeatable"
+    finally:
+        k3.k3moe_layer_free(L)
