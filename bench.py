@@ -1,21 +1,27 @@
 """Benchmark of the routed MXFP4 MoE layer on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl b300|reference]
-                    [--workload decode1|decode64|prefill4096] [--tokens-per-step M]
+                    [--workload all|decode1|decode64|prefill4096|stack4] [--tokens-per-step M]
 
-Default workload (decode1): one Kimi K3-shaped MoE layer (d=7168, f=1536, E=896, k=16),
-single-token decode, M=1000 seeded tokens per step run back to back as T=1 layer calls.
-A step is one pass of the whole hot path (router, top-k, bucketing, expert FFNs, combine)
-over those tokens.  The 15.7 GB expert pool is far larger than L2, so each token streams
-its 16 experts from HBM (the 25.7 MB router stays L2-resident across tokens, as it would in
-a real decode loop).
+Default (--workload all): one Kimi K3-shaped MoE layer (d=7168, f=1536, E=896, k=16).
+  headline  decode1: single-token decode, M=1000 seeded tokens per step run back to back as
+            T=1 layer calls.  A step is one pass of the whole hot path (router, top-k,
+            bucketing, expert FFNs, combine) over those tokens.  The 15.7 GB expert pool is far
+            larger than L2, so each token streams its 16 experts from HBM (the 25.7 MB router
+            stays L2-resident across tokens, as it would in a real decode loop).
+  configs   decode64: the same layer, M tokens per step in T=64 calls (batched decode);
+            prefill4096: a second layer with a +2.0 selection bias on 32 experts, one T=4096
+            call per step (tensor-core grouped GEMM path).
+Every workload reports tokens/s with inputs resident, the dominant kernel's roofline from an
+event-timed pass, e2e through the host-buffer C entry point (k3moe_layer_forward_host), and the
+oracle timed on the host cores at all threads and at one thread.
 
 Prints one JSON line.  With --gpus N > 1 (launched by torchrun) every rank runs an
 independent replica of the layer (the layer has no cross-GPU step on one node here);
 value = tokens of all ranks / max rank time.
 
 --impl reference times the CPU oracle (plain fp64 C, this repository's oracle/) on the
-host cores, on a bounded sample of the same workload.
+host cores, on a bounded sample of the single-token decode workload.
 """
 from __future__ import annotations
 
@@ -49,6 +55,15 @@ WORKLOADS = {
     "stack4": dict(T=1, desc="4 stacked K3 MoE layers (d=7168 f=1536 E=896 k=16; between them r=bf16(r+y), "
                              "next input RMSNorm(r)), "
                              "T=1 decode, 62.9 GB expert pool in pinned host memory behind a device LRU cache"),
+}
+
+
+L2_NOTE = {
+    "decode1": "inputs larger than L2: 15.7 GB expert pool streamed from HBM (16 experts, 281 MB per call); "
+               "router L2-resident",
+    "decode64": "inputs larger than L2: about 620 experts (10.9 GB) streamed per call; router L2-resident",
+    "prefill4096": "inputs larger than L2: 561 MB of hot experts, 58.7 MB of tokens and 1.9 GB of per-pick "
+                   "activations and outputs per call",
 }
 
 
@@ -183,27 +198,43 @@ def build_layer(torch, k3, T_max, bias=None, n_exp=E):
     return layer
 
 
-def run_b300(args):
-    import torch
-    import synth
-    import mxfp4_routed_expert_06_b300 as k3
+def _roofline(prof, T, distinct_per_call, hbm_peak, bf16_peak, peak_kind):
+    """Roofline of the dominant kernel from the event-timed pass: the gate/up GEMM (tensor
+    bound) on the tensor-core path, the gate/up streaming kernel (HBM bound) otherwise."""
+    if prof["gemm_gu"][1]:
+        gu_ms, gu_n = prof["gemm_gu"]
+        flops = 4.0 * F * D * T * K  # 4*f*d flops per pick (gate and up)
+        achieved = flops / (gu_ms / gu_n / 1e3) / 1e12
+        dn_ms, dn_n = prof["gemm_dn"]
+        return {"bound": "tensor", "kernel": "gemm_kernel<gate/up> (tcgen05, fp16 in, fp32 TMEM accumulate)",
+                "achieved": round(achieved, 1), "peak": bf16_peak, "unit": "TFLOP/s",
+                "frac": round(achieved / bf16_peak, 4),
+                "peak_kind": f"{peak_kind} (cuBLAS bf16 dense, burst; fp16 dense has the same rate)",
+                "algorithmic_flops_per_launch": flops,
+                "traffic": _traffic_from_profile("mxfp4_routed_expert_06_b300/csrc/gemm_tc.cu",
+                                                 "gemm_gu_prefill_k3_t4096.txt") if T == 4096 else None,
+                "down_gemm_tflops": round(2.0 * F * D * T * K / (dn_ms / dn_n / 1e3) / 1e12, 1)}
+    gu_ms, gu_n = prof["gateup"]
+    gu_bytes = distinct_per_call * GATEUP_BYTES  # each active expert's gate/up bytes once per call
+    achieved = gu_bytes / (gu_ms / gu_n / 1e3) / 1e9 if gu_n else None
+    summary = {1: "gateup_decode_k3_t1.txt", 64: "gateup_decode_k3_t64.txt"}.get(T)
+    traffic = _traffic_from_profile("mxfp4_routed_expert_06_b300/csrc/decode_ffn.cu", summary) if summary else None
+    dn_ms, dn_n = prof["down"]
+    return {"bound": "hbm", "kernel": "gateup_kernel (gate/up + SwiGLU, register decode)",
+            "achieved": None if achieved is None else round(achieved, 1),
+            "peak": hbm_peak, "unit": "GB/s",
+            "frac": None if achieved is None else round(achieved / hbm_peak, 4),
+            "peak_kind": f"{peak_kind} (HBM copy peak)",
+            "algorithmic_bytes_per_launch": int(gu_bytes), "traffic": traffic,
+            "down_kernel_gbs": round(distinct_per_call * DOWN_BYTES / (dn_ms / dn_n / 1e3) / 1e9, 1) if dn_n else None}
 
-    ws, rank = _dist()
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    pg = None
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-        pg = dist
-    wl = WORKLOADS[args.workload]
-    T = wl["T"]
-    bias = synth.hot_bias(SEED, 0, args.experts, 32, 2.0) if args.workload == "prefill4096" else None
-    layer = build_layer(torch, k3, max(T, 1), bias, args.experts)
-    calls = args.tokens_per_step if T == 1 else 1
+
+def measure(torch, k3, layer, T, calls, xs, args, pg, rank, peaks):
+    """Times `calls` back-to-back T-token layer calls per step (inputs resident), then the same
+    steps with an event pair around every launch (per-kernel durations), then end to end through
+    the host-buffer entry point (host copies inside every call).  Returns the numbers."""
+    hbm_peak, bf16_peak, peak_kind = peaks
     tokens_per_step = calls * T
-    # seeded tokens, distinct per rank
-    xs = synth.tokens_bf16(SEED, 0, rank * 10_000_000, tokens_per_step, D)
     xd = torch.from_numpy(xs.view(np.int16)).cuda()
     y = torch.empty((tokens_per_step, D), dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
@@ -214,7 +245,7 @@ def run_b300(args):
 
     for _ in range(args.warmup):
         step()
-    torch.cuda.synchronize()
+    k3.k3moe_sync(layer)
 
     def timed(n_steps):
         if pg:
@@ -230,9 +261,8 @@ def run_b300(args):
             pg.barrier()
         return e0.elapsed_time(e1)
 
-    clocks = ClockSampler(local)
-    clocks.start()
     ms = timed(args.steps)
+    k3.k3moe_sync(layer)  # any device-side wait that gave up would make the timing invalid
     # per-kernel durations: the same steps again with an event pair around every launch (the
     # events sit between kernels and stop programmatic launch overlap, so the headline timing
     # above runs without them)
@@ -240,120 +270,137 @@ def run_b300(args):
     ms_profiled = timed(args.steps)
     prof = k3.k3moe_profile_read(layer)
     k3.k3moe_profile(layer, False)
-    clk = clocks.stop()
     value, ms = job_throughput(tokens_per_step * args.steps, ms, pg)
 
     # distinct experts touched (algorithmic weight bytes): counted from the actual routing
     idx = torch.empty((tokens_per_step, K), dtype=torch.int32, device="cuda")
     w = torch.empty((tokens_per_step, K), dtype=torch.float32, device="cuda")
-    distinct = 0
     for c in range(calls):
         k3.k3moe_router_topk(layer, xd[c * T:(c + 1) * T], T, idx[c * T:(c + 1) * T], w[c * T:(c + 1) * T], stream)
     torch.cuda.synchronize()
     idx_h = idx.cpu().numpy()
-    for c in range(calls):
-        distinct += len(np.unique(idx_h[c * T:(c + 1) * T]))
+    distinct = sum(len(np.unique(idx_h[c * T:(c + 1) * T])) for c in range(calls))
     weight_bytes_per_step = distinct * EXPERT_BYTES
-
-    hbm_peak, bf16_peak, peak_kind = _peaks()
+    roofline = _roofline(prof, T, distinct / calls, hbm_peak, bf16_peak, peak_kind)
     launches = sum(v[1] for v in prof.values())
-    if prof["gemm_gu"][1]:
-        # tensor-core path: dominant kernel is the gate/up GEMM, 4*f*d flops per pick; fp16
-        # dense MMA runs at the bf16 rate, so the measured bf16 peak is the denominator
-        gu_ms, gu_n = prof["gemm_gu"]
-        flops = 4.0 * F * D * T * K
-        achieved = flops / (gu_ms / gu_n / 1e3) / 1e12
-        roofline = {"bound": "tensor", "kernel": "gemm_kernel<gate/up> (tcgen05, fp16 in, fp32 TMEM accumulate)",
-                    "achieved": round(achieved, 1), "peak": bf16_peak, "unit": "TFLOP/s",
-                    "frac": round(achieved / bf16_peak, 4),
-                    "peak_kind": f"{peak_kind} (cuBLAS bf16 dense, burst; fp16 dense has the same rate)",
-                    "algorithmic_flops_per_launch": flops,
-                    "traffic": _traffic_from_profile("mxfp4_routed_expert_06_b300/csrc/gemm_tc.cu",
-                                                     "gemm_gu_prefill_k3_t4096.txt") if T == 4096 else None}
-        dn_ms, dn_n = prof["gemm_dn"]
-        gemm_tflops = 6.0 * F * D * T * K / ((gu_ms / gu_n + dn_ms / dn_n) / 1e3) / 1e12
-    else:
-        # dominant kernel: gate/up (two thirds of the streamed expert bytes)
-        gu_ms, gu_n = prof["gateup"]
-        gu_bytes_per_launch = (distinct / calls) * GATEUP_BYTES
-        achieved = gu_bytes_per_launch / (gu_ms / gu_n / 1e3) / 1e9 if gu_n else None
-        # the committed capture is of a T=1 launch; other workloads have no capture of their own
-        traffic = (_traffic_from_profile("mxfp4_routed_expert_06_b300/csrc/decode_ffn.cu",
-                                         "gateup_decode_k3_t1.txt") if T == 1 else None)
-        roofline = {"bound": "hbm", "kernel": "gateup_kernel (gate/up + SwiGLU, register decode)",
-                    "achieved": None if achieved is None else round(achieved, 1),
-                    "peak": hbm_peak, "unit": "GB/s",
-                    "frac": None if achieved is None else round(achieved / hbm_peak, 4),
-                    "peak_kind": f"{peak_kind} (HBM copy peak)",
-                    "algorithmic_bytes_per_launch": int(gu_bytes_per_launch), "traffic": traffic}
-        gemm_tflops = None
 
-    # end to end (wall clock): every step copies its tokens from pinned host memory to the
-    # device, runs the layer calls through the public entry point, and reads the results back
+    # end to end through the C ABI with host buffers: every call copies its tokens from pinned
+    # host memory, runs the layer and copies y back before it returns
     xh = torch.from_numpy(xs.view(np.int16)).pin_memory()
     yh = torch.empty((tokens_per_step, D), dtype=torch.float32).pin_memory()
-    xe = torch.empty_like(xd)
-    ye = torch.empty_like(y)
 
     def e2e_step():
-        xe.copy_(xh, non_blocking=True)
         for c in range(calls):
-            k3.k3moe_layer_forward(layer, xe[c * T:(c + 1) * T], T, ye[c * T:(c + 1) * T], stream)
-        yh.copy_(ye, non_blocking=True)
-        torch.cuda.synchronize()
+            k3.k3moe_layer_forward_host(layer, xh[c * T:(c + 1) * T], T, yh[c * T:(c + 1) * T], stream)
 
     e2e_step()
     e2e_steps = max(1, min(args.steps, 3))
+    if pg:
+        pg.barrier()
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
         e2e_step()
     e2e_s = time.perf_counter() - t0
     e2e_val = job_rate_min(tokens_per_step * e2e_steps / e2e_s, pg)
-    # the host-buffer entry point, one synchronising call per T-token call (a caller that needs
-    # every result on the host before the next call)
-    for c in range(min(calls, 20)):
-        k3.k3moe_layer_forward_host(layer, xh[c * T:(c + 1) * T], T, yh[c * T:(c + 1) * T], stream)
-    t0 = time.perf_counter()
-    for c in range(calls):
-        k3.k3moe_layer_forward_host(layer, xh[c * T:(c + 1) * T], T, yh[c * T:(c + 1) * T], stream)
-    host_call_val = job_rate_min(tokens_per_step / (time.perf_counter() - t0), pg)
+    ms_step = ms / args.steps
+    return {
+        "value": round(value, 3), "unit": "tokens/s", "ms_per_step": round(ms_step, 4),
+        "calls_per_step": calls, "tokens_per_step": tokens_per_step, "us_per_call": round(1e3 * ms_step / calls, 2),
+        "weight_gbs": round(weight_bytes_per_step * args.steps * (pg.get_world_size() if pg else 1)
+                            / (ms / 1e3) / 1e9, 1),
+        "weight_pct_of_hbm_peak": round(100 * weight_bytes_per_step * args.steps / (ms / 1e3) / 1e9 / hbm_peak, 1),
+        "distinct_experts_per_call": round(distinct / calls, 2),
+        "roofline": roofline,
+        "kernel_ms_per_launch": {k: round(v[0] / v[1], 5) for k, v in prof.items() if v[1]},
+        "kernel_timing": f"event pairs around every launch, second pass of the same {args.steps} steps "
+                         f"({round(ms_profiled / args.steps, 4)} ms/step with the events in place)",
+        "gpu_launches": int(launches),
+        "e2e": {"value": round(e2e_val, 3), "unit": "tokens/s",
+                "h2d_bytes_per_step": tokens_per_step * D * 2, "d2h_bytes_per_step": tokens_per_step * D * 4,
+                "timing": f"wall clock of {e2e_steps} steps, each {calls} calls of k3moe_layer_forward_host "
+                          f"(C ABI, host buffers: H2D of x from pinned memory, the layer, D2H of y, one "
+                          f"synchronisation per call)"},
+    }
+
+
+def run_b300(args):
+    import torch
+    import synth
+    import mxfp4_routed_expert_06_b300 as k3
+
+    ws, rank = _dist()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        pg = dist
+    peaks = _peaks()
+    # the headline workload first, then (default run) the metric's other two token counts
+    names = ["decode1", "decode64", "prefill4096"] if args.workload == "all" else [args.workload]
+    clocks = ClockSampler(local)
+    clocks.start()
+    results = {}
+    layer, layer_kind = None, None
+    for name in names:
+        T = WORKLOADS[name]["T"]
+        kind = "prefill" if name == "prefill4096" else "decode"
+        if layer_kind != kind:
+            if layer is not None:
+                k3.k3moe_layer_free(layer)
+                torch.cuda.empty_cache()
+            bias = synth.hot_bias(SEED, 0, args.experts, 32, 2.0) if kind == "prefill" else None
+            layer = build_layer(torch, k3, 4096 if kind == "prefill" else 64, bias, args.experts)
+            layer_kind = kind
+        if T == 1:
+            calls = args.tokens_per_step
+        elif T == 64:
+            calls = max(1, args.tokens_per_step // 64)
+        else:
+            calls = 1
+        # seeded tokens, distinct per rank and per workload
+        xs = synth.tokens_bf16(SEED, 0, rank * 10_000_000 + 1_000_000 * len(results), calls * T, D)
+        results[name] = measure(torch, k3, layer, T, calls, xs, args, pg, rank, peaks)
+    clk = clocks.stop()
+    k3.k3moe_layer_free(layer)
 
     out = None
     if rank == 0:
+        head_name = names[0]
+        head = results[head_name]
         cpu = None
         if ws == 1 and not args.no_cpu_baseline:
-            cpu = cpu_baseline(args, seconds=args.cpu_seconds)
+            cpu = {n: cpu_baselines(n, args.cpu_seconds) for n in names}
         out = {
-            "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
+            "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "mxfp4 weights -> f16 mma, f32 accumulate",
             "data": "synthetic (seeded splitmix64 experts, N(0,1) bf16 tokens, N(0,1/d) router)",
             "impl": "b300",
-            "config": {"workload": wl["desc"] + ("" if args.experts == E else
-                                                 f" [profiling case: only {args.experts} experts resident]"),
-                       "calls_per_step": calls, "tokens_per_step": tokens_per_step,
+            "config": {"workload": WORKLOADS[head_name]["desc"] + ("" if args.experts == E else
+                                                                   f" [profiling case: only {args.experts} "
+                                                                   f"experts resident]"),
+                       "calls_per_step": head["calls_per_step"], "tokens_per_step": head["tokens_per_step"],
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                       "l2": ("inputs larger than L2: 15.7 GB expert pool streamed from HBM; router L2-resident"
-                              if T < 4096 else "inputs larger than L2: 561 MB of hot experts, 1.9 GB of per-pick "
-                              "activations and outputs per call")},
-            "weight_gbs": round(weight_bytes_per_step * args.steps * ws / (ms / 1e3) / 1e9, 1),
-            "weight_pct_of_hbm_peak": round(100 * weight_bytes_per_step * args.steps / (ms / 1e3) / 1e9 / hbm_peak, 1),
-            "distinct_experts_per_call": round(distinct / calls, 2),
-            "roofline": roofline,
-            "expert_gemm_tflops": None if gemm_tflops is None else round(gemm_tflops, 1),
-            "kernel_ms_per_launch": {k: round(v[0] / v[1], 5) for k, v in prof.items() if v[1]},
-            "kernel_timing": f"event pairs around every launch, second pass of the same {args.steps} steps "
-                             f"({round(ms_profiled / args.steps, 4)} ms/step with the events in place)",
-            "gpu_launches": int(launches),
-            "e2e": {"value": round(e2e_val, 3), "unit": "tokens/s",
-                    "h2d_bytes_per_step": tokens_per_step * D * 2, "d2h_bytes_per_step": tokens_per_step * D * 4,
-                    "timing": "wall clock per step: pinned H2D of the step's tokens, the layer calls, D2H of y, "
-                              "synchronise",
-                    "host_entry_per_call": round(host_call_val, 3)},
-            "clocks": clk,
-            "cpu_baseline": cpu,
+                       "l2": L2_NOTE[head_name]},
         }
-    k3.k3moe_layer_free(layer)
+        for key in ("weight_gbs", "weight_pct_of_hbm_peak", "distinct_experts_per_call", "roofline",
+                    "kernel_ms_per_launch", "kernel_timing", "gpu_launches", "e2e"):
+            out[key] = head[key]
+        out["clocks"] = clk
+        out["cpu_baseline"] = None if cpu is None else cpu[head_name]["all_cores"]
+        if len(names) > 1:
+            out["gpu_launches"] = int(sum(results[n]["gpu_launches"] for n in names))
+            out["configs"] = {}
+            for n in names:
+                r = dict(results[n])
+                r["workload"] = WORKLOADS[n]["desc"]
+                r["l2"] = L2_NOTE[n]
+                r["cpu_baseline"] = None if cpu is None else cpu[n]
+                out["configs"][n] = r
+        elif cpu is not None:
+            out["cpu_baseline_1thread"] = cpu[head_name]["one_thread"]
     if pg:
         pg.destroy_process_group()
     return out
@@ -519,31 +566,85 @@ def _oracle_tokens(n_tokens, rank_offset=0):
     for t in range(n_tokens):
         t0 = time.perf_counter()
         idx, w, _, _ = oracle.router(xs[t:t + 1], Wr, None, K)
+        oracle.bucket(idx, E)
         t_total += time.perf_counter() - t0
-        nibs, scls = [], []
-        for e in idx[0].tolist():
-            n, s = synth.experts(SEED, 0, e, e + 1, D, F)
-            nibs.append(n[0])
-            scls.append(s[0])
+        nibs, scls = _expert_blocks(idx[0])
         t0 = time.perf_counter()
         oracle.moe(xs[t:t + 1], w, nibs, scls, F)
         t_total += time.perf_counter() - t0
     return t_total, oracle.max_threads()
 
 
-def cpu_baseline(args, seconds=20.0):
-    """The oracle as it stands, on a bounded sample of the decode workload."""
+def _expert_blocks(ids, seed=SEED):
+    import synth
+    nibs, scls = [], []
+    for e in ids.tolist():
+        n, s = synth.experts(seed, 0, e, e + 1, D, F)
+        nibs.append(n[0])
+        scls.append(s[0])
+    return nibs, scls
+
+
+def _oracle_batch(router_tokens, y_seconds, bias=None):
+    """The oracle on one multi-token call, sampled: router + top-k and bucketing on router_tokens
+    tokens (timed once), then the expert FFNs and combine token by token until y_seconds of FFN
+    time have passed (at least one token).  Tokens are independent, so seconds per token =
+    router part / router_tokens + FFN part / FFN tokens.  Returns (seconds per token, threads,
+    FFN tokens)."""
+    import oracle
+    import synth
+    Wr = synth.router_weights(SEED, 0, E, D)
+    xs = synth.tokens_bf16(SEED, 0, 5_000_000, router_tokens, D)
+    t0 = time.perf_counter()
+    idx, w, _, _ = oracle.router(xs, Wr, bias, K)
+    oracle.bucket(idx, E)
+    t_router = time.perf_counter() - t0
+    t_ffn, n_y = 0.0, 0
+    while n_y < router_tokens and (n_y == 0 or t_ffn < y_seconds):
+        nibs, scls = _expert_blocks(idx[n_y])
+        t0 = time.perf_counter()
+        oracle.moe(xs[n_y:n_y + 1], w[n_y:n_y + 1], nibs, scls, F)
+        t_ffn += time.perf_counter() - t0
+        n_y += 1
+    return t_router / router_tokens + t_ffn / n_y, oracle.max_threads(), n_y
+
+
+def _one_cpu_baseline(name, threads, seconds):
     import oracle
     oracle.build()
-    n = 1
-    sec, cores = _oracle_tokens(n)
-    while sec < seconds * 0.5 and n < 64:
-        n2 = max(1, int(n * seconds / max(sec, 1e-3) * 0.5))
-        s2, _ = _oracle_tokens(n2, 100 + n)
-        n, sec = n2, s2
-    return {"value": round(n / sec, 6), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{n} single-token K3 layer calls (router over 896 experts + 16 expert FFNs each), "
-                      f"fp64 scalar MXFP4 decode, {sec:.1f} s"}
+    oracle.set_threads(threads)
+    try:
+        if name == "decode1":
+            n = 1
+            sec, cores = _oracle_tokens(n)
+            if sec < seconds * 0.5:
+                n = max(1, min(64, int(n * seconds * 0.5 / max(sec, 1e-3))))
+                sec, cores = _oracle_tokens(n, 100)
+            return {"value": round(n / sec, 6), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                    "sample": f"{n} single-token K3 layer calls (router over 896 experts, top-16, bucketing and "
+                              f"16 expert FFNs each), fp64 scalar MXFP4 decode, {sec:.1f} s"}
+        T = WORKLOADS[name]["T"]
+        bias = synth_bias() if name == "prefill4096" else None
+        r_tok = T if threads > 1 else min(T, 64)
+        per_tok, cores, n_y = _oracle_batch(r_tok, seconds * 0.5, bias)
+        return {"value": round(1.0 / per_tok, 6), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                "sample": f"one {T}-token call sampled: router, top-16 and bucketing on {r_tok} tokens, the "
+                          f"16 expert FFNs and combine on {n_y} of them; seconds per token = router part / "
+                          f"{r_tok} + FFN part / {n_y} (tokens are independent, so the whole call "
+                          f"extrapolates linearly); fp64 scalar MXFP4 decode"}
+    finally:
+        oracle.set_threads(os.cpu_count() or 1)
+
+
+def synth_bias():
+    import synth
+    return synth.hot_bias(SEED, 0, E, 32, 2.0)
+
+
+def cpu_baselines(name, seconds):
+    """The oracle as it stands, on bounded samples of the workload: all host cores, then 1 thread."""
+    return {"all_cores": _one_cpu_baseline(name, os.cpu_count() or 1, seconds),
+            "one_thread": _one_cpu_baseline(name, 1, seconds / 2)}
 
 
 def run_reference(args):
@@ -582,9 +683,11 @@ def main():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="b300", choices=["b300", "reference"])
-    ap.add_argument("--workload", default="decode1", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="all", choices=["all"] + sorted(WORKLOADS),
+                    help="all (default): the single-token decode headline, then T=64 and T=4096 under 'configs'")
     ap.add_argument("--tokens-per-step", type=int, default=None,
-                    help="T=1 calls per step (default 1000; 256 for stack4)")
+                    help="tokens per step of the decode workloads: T=1 calls (default 1000; 256 for stack4); "
+                         "the T=64 workload runs this many tokens in T=64 calls")
     ap.add_argument("--budget-gb", type=float, default=8.0, help="stack4: device cache budget (1 GB = 1e9 B)")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

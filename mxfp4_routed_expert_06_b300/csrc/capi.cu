@@ -114,6 +114,7 @@ struct k3moe_layer {
   cudaEvent_t copies_done = nullptr;
   uint16_t* x_stage = nullptr;  // forward_host staging
   float* y_stage = nullptr;
+  uint32_t* flags_host = nullptr;  // pinned: device error flags read back by forward_host
   int num_sms = 148;
   unsigned long long wait_ns = 2000000000ull;  // bound on device-side waits
   int test_stall = 0;                           // next forward stalls its FFN consumers (timeout test)
@@ -240,6 +241,7 @@ void free_layer(k3moe_layer* L) {
   cudaFree(L->ws_block);
   cudaFree(L->x_stage);
   cudaFree(L->y_stage);
+  cudaFreeHost(L->flags_host);
   for (auto& t : L->timed) {
     cudaEventDestroy(t.a);
     cudaEventDestroy(t.b);
@@ -760,7 +762,8 @@ int k3moe_layer_forward_host(k3moe_layer* L, const void* x_host, int T, float* y
   const k3moe_dims& D = L->dims;
   if (!L->x_stage) {
     if (cudaMalloc(&L->x_stage, (size_t)D.T_max * D.d * 2) != cudaSuccess ||
-        cudaMalloc(&L->y_stage, (size_t)D.T_max * D.d * 4) != cudaSuccess) {
+        cudaMalloc(&L->y_stage, (size_t)D.T_max * D.d * 4) != cudaSuccess ||
+        cudaHostAlloc((void**)&L->flags_host, 16, cudaHostAllocDefault) != cudaSuccess) {
       cudaGetLastError();
       return fail(K3MOE_ERR_OOM, "host-forward staging allocation failed");
     }
@@ -770,9 +773,10 @@ int k3moe_layer_forward_host(k3moe_layer* L, const void* x_host, int T, float* y
   int rc = forward_impl(L, L->x_stage, T, L->y_stage, s);
   if (rc) return rc;
   CUDA_TRY(cudaMemcpyAsync(y_host, L->y_stage, (size_t)T * D.d * 4, cudaMemcpyDeviceToHost, s));
+  // the error flags come back on the same stream, so one synchronisation covers both copies
+  CUDA_TRY(cudaMemcpyAsync(L->flags_host, L->ws.sync + 1, 4, cudaMemcpyDeviceToHost, s));
   CUDA_TRY(cudaStreamSynchronize(s));
-  uint32_t flags = 0;
-  CUDA_TRY(cudaMemcpy(&flags, L->ws.sync + 1, 4, cudaMemcpyDeviceToHost));
+  const uint32_t flags = *reinterpret_cast<volatile uint32_t*>(L->flags_host);
   if (flags) {
     CUDA_TRY(reset_after_timeout(L));
     return fail(K3MOE_ERR_TIMEOUT, "a device-side wait gave up (flags 0x%x)", flags);
