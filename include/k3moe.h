@@ -104,7 +104,7 @@ int k3moe_pack_experts(const k3moe_dims* dims, const void* canon_nib, const void
  *   logit[t,e] = sum_j x[t,j]*W_r[e,j] (fp32 accumulate), sigma = 1/(1+exp(-logit)),
  *   key = sigma + bias[e]; idx[t,:] = the k experts with the largest keys in descending key
  *   order, ties to the lower expert id; w[t,i] = sigma[idx[t,i]] / sum_i sigma[idx[t,i]].
- *   x    device pointer, [T][d] bf16, row-major
+ *   x    device pointer, [T][d] bf16, row-major, 16-byte aligned
  *   T    1..T_max
  *   idx  device pointer, [T][k] int32 (output)
  *   w    device pointer, [T][k] float32 (output)
@@ -154,7 +154,7 @@ int k3moe_bucket(k3moe_layer* layer, const int32_t* idx, int T, int32_t* counts,
  * weights -> combine ("four reductions", reduction 1; invariants row 5):
  *   y[t,:] = sum_{slot=0..k-1} w[t,slot] * W_d,e (silu(W_g,e x_t) * (W_u,e x_t)),
  *   e = idx[t,slot], silu(z) = z/(1+exp(-z)), summed in slot order.
- *   x  device pointer, [T][d] bf16 row-major;  y  device pointer, [T][d] float32 (output).
+ *   x  device pointer, [T][d] bf16 row-major, 16-byte aligned;  y  device pointer, [T][d] float32 (output).
  *   T  1..T_max.  y excludes any residual.
  * The result does not depend on the cache budget, on which experts were resident, or on
  * the run (bitwise).  Small T runs the register-decode path, large T the tcgen05 grouped
