@@ -10,10 +10,12 @@ cites the passage of the pages it follows).  This module only builds the library
 and marshals numpy arrays.
 
 Parity pins (tests that tie the oracle to something other than itself) are in
-``tests/test_oracle_pins.py``.  Every oracle function is pinned; none is
-"parity unpinned" except the end-to-end y values of full-size layers, which the
-pages never print (they are pinned through the per-step pins and the second
-formulation of the FFN).
+``tests/test_oracle_pins.py``.  Every oracle function is pinned, with two exceptions:
+the end-to-end y values of full-size layers, which the pages never print (they are
+pinned through the per-step pins and the second formulation of the FFN), and the
+SiTU-GLU gate (``situ``, act = 1): parity unpinned, because the pages give only its
+ingredients (tanh, sigmoid) and its bound (beta1 * beta2 = 100), not its formula; the
+pins check the bound and the properties of the reading written in k3oracle.c.
 """
 from __future__ import annotations
 
@@ -53,8 +55,9 @@ def _L():
         lib.k3o_router.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]
         lib.k3o_router.restype = None
         lib.k3o_bucket.argtypes, lib.k3o_bucket.restype = [i32, i32, i32, vp, vp, vp, vp], None
-        lib.k3o_expert_ffn.argtypes, lib.k3o_expert_ffn.restype = [i32, i32, vp, vp, vp, vp, vp, vp], None
-        lib.k3o_moe.argtypes, lib.k3o_moe.restype = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp], None
+        lib.k3o_expert_ffn.argtypes, lib.k3o_expert_ffn.restype = [i32, i32, vp, vp, vp, vp, vp, vp, i32], None
+        lib.k3o_moe.argtypes, lib.k3o_moe.restype = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i32], None
+        lib.k3o_situ.argtypes, lib.k3o_situ.restype = [d], d
         lib.k3o_bf16_rne.argtypes, lib.k3o_bf16_rne.restype = [ctypes.c_float], ctypes.c_uint16
         lib.k3o_residual_rmsnorm.argtypes = [i32, i32, vp, vp, d, vp, vp]
         lib.k3o_residual_rmsnorm.restype = None
@@ -134,17 +137,25 @@ def bucket(idx, E: int):
     return counts, offsets, perm
 
 
-def expert_ffn(d: int, f: int, nib, scl, x):
+ACT_SWIGLU, ACT_SITU_GLU = 0, 1
+
+
+def situ(z: float) -> float:
+    """The SiTU-GLU gate as this oracle reads it (parity unpinned: see k3oracle.c)."""
+    return _L().k3o_situ(z)
+
+
+def expert_ffn(d: int, f: int, nib, scl, x, act: int = ACT_SWIGLU):
     """One expert on one token (x as float64[d]) -> (h[f], o[d], a[d])."""
     nib, scl, x = _c(nib, np.uint8), _c(scl, np.uint8), _c(x, np.float64)
     h = np.empty(f, np.float64)
     o = np.empty(d, np.float64)
     a = np.empty(d, np.float64)
-    _L().k3o_expert_ffn(d, f, _p(nib), _p(scl), _p(x), _p(h), _p(o), _p(a))
+    _L().k3o_expert_ffn(d, f, _p(nib), _p(scl), _p(x), _p(h), _p(o), _p(a), act)
     return h, o, a
 
 
-def moe(x_bits, w, pick_nib: list, pick_scl: list, f: int):
+def moe(x_bits, w, pick_nib: list, pick_scl: list, f: int, act: int = ACT_SWIGLU):
     """Combine of the T*k picks.  pick_nib[p]/pick_scl[p]: canonical block of the
     expert of pick p = t*k + slot.  -> (y float64[T,d], sumabs float64[T,d])."""
     x_bits = _c(x_bits, np.uint16)
@@ -157,18 +168,19 @@ def moe(x_bits, w, pick_nib: list, pick_scl: list, f: int):
     sptr = (ctypes.c_void_p * (T * k))(*[a.ctypes.data for a in keep[T * k:]])
     y = np.empty((T, d), np.float64)
     sumabs = np.empty((T, d), np.float64)
-    _L().k3o_moe(T, d, f, k, _p(x_bits), _p(w), ctypes.addressof(nptr), ctypes.addressof(sptr), _p(y), _p(sumabs))
+    _L().k3o_moe(T, d, f, k, _p(x_bits), _p(w), ctypes.addressof(nptr), ctypes.addressof(sptr), _p(y), _p(sumabs),
+                 act)
     del keep
     return y, sumabs
 
 
-def layer(x_bits, Wr, bias, k: int, f: int, nib_all, scl_all):
+def layer(x_bits, Wr, bias, k: int, f: int, nib_all, scl_all, act: int = ACT_SWIGLU):
     """The whole layer for configs whose experts fit in host memory.
     nib_all/scl_all: canonical blocks of all E experts, [E, ...]."""
     idx, w, logits, keys = router(x_bits, Wr, bias, k)
     counts, offsets, perm = bucket(idx, Wr.shape[0])
     flat = idx.reshape(-1)
-    y, sumabs = moe(x_bits, w, [nib_all[e] for e in flat], [scl_all[e] for e in flat], f)
+    y, sumabs = moe(x_bits, w, [nib_all[e] for e in flat], [scl_all[e] for e in flat], f, act)
     return dict(idx=idx, w=w, logits=logits, keys=keys, counts=counts, offsets=offsets, perm=perm, y=y,
                 sumabs=sumabs)
 

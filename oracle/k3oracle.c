@@ -164,16 +164,31 @@ void k3o_bucket(int T, int k, int E, const int32_t* idx, int32_t* counts, int32_
 
 static double silu(double z) { return z / (1.0 + exp(-z)); }
 
+/* SiTU-GLU gate ("kimi-k3-in-c deep dive", glossary entry SiTU-GLU: K3's activation, a
+ * combination of tanh and sigmoid whose parameters beta1 = 4 and beta2 = 25 bound the gate
+ * above by 100).  The pages print no formula.  READING (parity unpinned: only the bound
+ * 100 = beta1 * beta2 and the two functions come from the page):
+ *   situ(z) = beta1 * beta2 * sigmoid(z) * tanh(z / beta2)
+ * which rises to beta1 * beta2 = 100 as z -> +inf, falls to 0 as z -> -inf, and has slope
+ * beta1 / 2 at 0; h = situ(g) * u replaces silu(g) * u. */
+static const double kSituBeta1 = 4.0, kSituBeta2 = 25.0;
+static double situ(double z) { return kSituBeta1 * kSituBeta2 * (1.0 / (1.0 + exp(-z))) * tanh(z / kSituBeta2); }
+double k3o_situ(double z) { return situ(z); }
+
+/* Gate activation: act 0 = SwiGLU's silu, act 1 = SiTU-GLU's situ (above). */
+static double gate_act(double z, int act) { return act == 1 ? situ(z) : silu(z); }
+
 /* One expert applied to one token, with SwiGLU (the activation the layer
- * specification names; READING: no clamp, no extra scaling):
+ * specification names; READING: no clamp, no extra scaling), or SiTU-GLU when act = 1:
  *   g_r = sum_j W_g[r,j] x_j,  u_r = sum_j W_u[r,j] x_j      (r < f, j < d)
- *   h_r = silu(g_r) * u_r,     silu(z) = z / (1 + exp(-z))
+ *   h_r = silu(g_r) * u_r,     silu(z) = z / (1 + exp(-z))     (act 0)
+ *   h_r = situ(g_r) * u_r                                      (act 1)
  *   o_i = sum_r W_d[i,r] h_r                                 (i < d)
  *   a_i = sum_r |W_d[i,r] h_r|     (magnitude of the terms, for error bounds)
  * nib/scl point at the expert's canonical block (three matrices back to back).
  * h (f values) and a (d values) may be NULL. */
 void k3o_expert_ffn(int d, int f, const uint8_t* nib, const uint8_t* scl, const double* x, double* h_out,
-                    double* o, double* a) {
+                    double* o, double* a, int act) {
   const size_t mn = (size_t)f * d / 2, ms = (size_t)f * d / 32;
   const uint8_t *ng = nib, *nu = nib + mn, *nd = nib + 2 * mn;
   const uint8_t *sg = scl, *su = scl + ms, *sd = scl + 2 * ms;
@@ -184,7 +199,7 @@ void k3o_expert_ffn(int d, int f, const uint8_t* nib, const uint8_t* scl, const 
       g += k3o_mx_elem(ng, sg, d, r, j) * x[j];
       u += k3o_mx_elem(nu, su, d, r, j) * x[j];
     }
-    h[r] = silu(g) * u;
+    h[r] = gate_act(g, act) * u;
     if (h_out) h_out[r] = h[r];
   }
   for (int i = 0; i < d; ++i) {
@@ -208,9 +223,9 @@ void k3o_expert_ffn(int d, int f, const uint8_t* nib, const uint8_t* scl, const 
  * pick_nib[p]/pick_scl[p] point at the canonical block of the expert routed by
  * pick p = t*k + slot (the caller resolves idx to expert storage).  The expert
  * FFNs of the T*k picks are independent and run in parallel; the sums over slots
- * run in the fixed order above. */
+ * run in the fixed order above.  act selects the gate activation (k3o_expert_ffn). */
 void k3o_moe(int T, int d, int f, int k, const uint16_t* x, const double* w, const uint8_t* const* pick_nib,
-             const uint8_t* const* pick_scl, double* y, double* sumabs) {
+             const uint8_t* const* pick_scl, double* y, double* sumabs, int act) {
   const int P = T * k;
   double* o = (double*)malloc(sizeof(double) * (size_t)P * d);
   double* a = (double*)malloc(sizeof(double) * (size_t)P * d);
@@ -221,7 +236,7 @@ void k3o_moe(int T, int d, int f, int k, const uint16_t* x, const double* w, con
     for (int p = 0; p < P; ++p) {
       const int t = p / k;
       for (int j = 0; j < d; ++j) xt[j] = k3o_bf16(x[(size_t)t * d + j]);
-      k3o_expert_ffn(d, f, pick_nib[p], pick_scl[p], xt, NULL, o + (size_t)p * d, a + (size_t)p * d);
+      k3o_expert_ffn(d, f, pick_nib[p], pick_scl[p], xt, NULL, o + (size_t)p * d, a + (size_t)p * d, act);
     }
     free(xt);
   }

@@ -366,3 +366,65 @@ def test_rmsnorm_scale_invariance_and_unit_rms():
     assert np.array_equal(a, b)
     v = synth.bf16_bits_to_f32(a).astype(np.float64)
     assert abs(np.mean(v * v) - 1.0) < 2 * 2 ** -8
+
+
+# ------------------------------------------------------------------ SiTU-GLU ---
+# The deep dive's glossary entry SiTU-GLU gives K3's activation only as a tanh-sigmoid
+# combination whose beta1 = 4 and beta2 = 25 bound the gate above by 100.  The formula is a
+# reading (parity unpinned); these pins tie the oracle to what the page fixes (the bound 100)
+# and to the limits and slope that the reading implies, and check where the gate sits in the FFN.
+
+def test_situ_bound_is_beta1_times_beta2():
+    assert oracle.situ(1000.0) == pytest.approx(100.0, rel=1e-15)   # beta1 * beta2, from the page
+    zs = np.linspace(-300.0, 300.0, 6001)
+    vals = np.array([oracle.situ(z) for z in zs])
+    assert vals.max() <= 100.0 and oracle.situ(200.0) > 99.9999
+
+
+def test_situ_limits_and_slope():
+    assert oracle.situ(0.0) == 0.0
+    assert abs(oracle.situ(-1000.0)) < 1e-300                        # sigmoid -> 0
+    eps = 1e-6
+    slope = (oracle.situ(eps) - oracle.situ(-eps)) / (2 * eps)
+    assert slope == pytest.approx(4.0 / 2.0, rel=1e-9)               # beta1 * beta2 * (1/2) * (1/beta2)
+    # for large positive gates the sigmoid is 1 and the gate is the capped tanh: 100 tanh(z / 25)
+    assert oracle.situ(50.0) == pytest.approx(100.0 * np.tanh(2.0), rel=1e-15)
+
+
+def test_ffn_situ_gate_applies_to_g_not_u():
+    # single nonzero weights (the closed-form case above): h = situ(g) * u with g = 2, u = 6
+    d, f = 64, 32
+    r0, j0, j1, i0 = 5, 7, 40, 50
+    ng = np.zeros((f, d // 2), np.uint8)
+    nu = np.zeros((f, d // 2), np.uint8)
+    nd = np.zeros((d, f // 2), np.uint8)
+    ng[r0, j0 // 2] = 0x2 << (4 * (j0 % 2))      # W_g[r0, j0] = 1.0
+    nu[r0, j1 // 2] = 0x4 << (4 * (j1 % 2))      # W_u[r0, j1] = 2.0
+    nd[i0, r0 // 2] = 0x9 << (4 * (r0 % 2))      # W_d[i0, r0] = -0.5
+    sg = np.full((f, d // 32), 127, np.uint8)
+    su = np.full((f, d // 32), 127, np.uint8)
+    sd = np.full((d, f // 32), 127, np.uint8)
+    nib, scl = _expert_blocks([ng, nu, nd], [sg, su, sd])
+    x = np.zeros(d)
+    x[j0], x[j1] = 2.0, 3.0
+    h, o, _ = oracle.expert_ffn(d, f, nib, scl, x, act=oracle.ACT_SITU_GLU)
+    assert h[r0] == pytest.approx(oracle.situ(2.0) * 6.0, rel=1e-15)
+    assert np.count_nonzero(h) == 1
+    assert o[i0] == pytest.approx(-0.5 * oracle.situ(2.0) * 6.0, rel=1e-15)
+
+
+def test_ffn_situ_second_formulation():
+    d, f = 256, 128
+    nib, scl = synth.experts(2, 0, 0, 2, d, f)
+    x = synth.bf16_bits_to_f32(synth.tokens_bf16(2, 0, 0, 1, d))[0].astype(np.float64)
+    mn, ms = f * d // 2, f * d // 32
+    situ = np.vectorize(oracle.situ)
+    for e in range(2):
+        Wg = oracle.decode_matrix(nib[e, :mn], scl[e, :ms], f, d)
+        Wu = oracle.decode_matrix(nib[e, mn:2 * mn], scl[e, ms:2 * ms], f, d)
+        Wd = oracle.decode_matrix(nib[e, 2 * mn:], scl[e, 2 * ms:], d, f)
+        h_ref = situ(Wg @ x) * (Wu @ x)
+        o_ref = Wd @ h_ref
+        h, o, a = oracle.expert_ffn(d, f, nib[e], scl[e], x, act=oracle.ACT_SITU_GLU)
+        np.testing.assert_allclose(h, h_ref, rtol=1e-12, atol=1e-12 * np.abs(h_ref).max())
+        assert np.all(np.abs(o - o_ref) <= 1e-12 * (np.abs(Wd) @ np.abs(h_ref)) + 1e-12)
