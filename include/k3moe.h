@@ -191,9 +191,27 @@ int k3moe_sync(k3moe_layer* layer);
                                    failure without copying (failure-path test).  That forward returns
                                    K3MOE_ERR_CUDA; the slot it was filling is forgotten, so later
                                    calls copy the expert again and their results are unchanged */
+#define K3MOE_OPT_ACTIVATION 8   /* value: K3MOE_ACT_SWIGLU (default) or K3MOE_ACT_SITU_GLU */
+#define K3MOE_OPT_MISS_PATH 9    /* cache mode: how a call's missed experts reach their slots.
+                                    K3MOE_MISS_COPY_ENGINE (default): one cudaMemcpyAsync per miss
+                                    on the cache's copy stream.  K3MOE_MISS_ZERO_COPY: one kernel on
+                                    the layer's stream copies every miss of the call, the SMs
+                                    reading the mapped pinned pool directly.  The output does not
+                                    depend on the choice (the FFN reads the slots either way) */
+#define K3MOE_MISS_COPY_ENGINE 0
+#define K3MOE_MISS_ZERO_COPY 1
 #define K3MOE_PATH_AUTO 0
 #define K3MOE_PATH_DECODE 1
 #define K3MOE_PATH_GEMM 2
+/* Gate activations (h = act(g) * u in every expert):
+ *   K3MOE_ACT_SWIGLU    act(g) = silu(g) = g / (1 + exp(-g)), the activation the layer specification names
+ *   K3MOE_ACT_SITU_GLU  act(g) = beta1 * beta2 * sigmoid(g) * tanh(g / beta2), beta1 = 4, beta2 = 25.
+ *                       The kimi-k3-in-c deep dive (glossary entry SiTU-GLU) names K3's activation as a
+ *                       tanh-sigmoid combination whose beta1 = 4 and beta2 = 25 bound the gate above by
+ *                       100; it prints no formula, so this one is a reading: it is bounded by
+ *                       beta1 * beta2 = 100, tends to 0 as g -> -inf and has slope beta1 / 2 at 0. */
+#define K3MOE_ACT_SWIGLU 0
+#define K3MOE_ACT_SITU_GLU 1
 int k3moe_set_option(k3moe_layer* layer, int option, long long value);
 
 /* Per-kernel device times (CUDA events around each launch, on the launch stream).

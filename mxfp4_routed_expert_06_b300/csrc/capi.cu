@@ -91,7 +91,11 @@ struct k3moe_layer {
   k3moe_dims dims{};
   size_t exp_bytes = 0;
   uint8_t* packed = nullptr;    // device, E * exp_bytes (device mode)
-  uint8_t* pool = nullptr;      // pinned host, E * exp_bytes (cache mode)
+  uint8_t* pool = nullptr;      // pinned host, E * exp_bytes (cache mode); mapped
+  uint8_t* pool_dev = nullptr;  // the pool's device address (zero-copy miss path)
+  MissCopy* miss_host = nullptr;  // pinned [E]: a call's misses (zero-copy miss path)
+  MissCopy* miss_dev = nullptr;   // device [E]
+  int miss_path = K3MOE_MISS_COPY_ENGINE;
   float* Wr = nullptr;          // device [E][d]
   uint16_t* Wsplit = nullptr;   // device [E][2d] bf16: W_r rounded (hi) then the rounding remainder (lo)
   float* bias = nullptr;        // device [E] or nullptr
@@ -122,6 +126,7 @@ struct k3moe_layer {
   int ring_depth = 0;                           // 0: automatic
   bool zero_scales = false;                     // some E8M0 scale byte is 0 (2^-127, a subnormal)
   int s_min = 255, s_max = 0;                   // range of the layer's scale bytes
+  int activation = K3MOE_ACT_SWIGLU;            // gate activation of every expert
 };
 
 namespace {
@@ -232,6 +237,8 @@ void free_layer(k3moe_layer* L) {
   if (L->last_stream) cudaStreamSynchronize(L->last_stream);
   cudaFree(L->packed);
   cudaFreeHost(L->pool);
+  cudaFreeHost(L->miss_host);
+  cudaFree(L->miss_dev);
   cudaFree(L->Wr);
   cudaFree(L->Wsplit);
   cudaFree(L->bias);
@@ -343,10 +350,19 @@ int make_resident(k3moe_layer* L, cudaStream_t s) {
     cudaEvent_t a, b;
     if (!C->free_events.empty()) { a = C->free_events.back(); C->free_events.pop_back(); } else cudaEventCreate(&a);
     if (!C->free_events.empty()) { b = C->free_events.back(); C->free_events.pop_back(); } else cudaEventCreate(&b);
-    // the copy stream must not overwrite a slot that earlier queued work on `s` may still read
-    CUDA_TRY(cudaEventRecord(L->copies_done, s));
-    CUDA_TRY(cudaStreamWaitEvent(C->copy_stream, L->copies_done, 0));
-    CUDA_TRY(cudaEventRecord(a, C->copy_stream));
+    const bool zc = L->miss_path == K3MOE_MISS_ZERO_COPY;
+    if (zc) {
+      // the copy kernel runs on `s` itself, after every earlier use of the slots on `s`
+      CUDA_TRY(cudaEventRecord(a, s));
+    } else {
+      // the copy stream must not overwrite a slot that earlier queued work on `s` may still read
+      CUDA_TRY(cudaEventRecord(L->copies_done, s));
+      CUDA_TRY(cudaStreamWaitEvent(C->copy_stream, L->copies_done, 0));
+      CUDA_TRY(cudaEventRecord(a, C->copy_stream));
+    }
+    int nm = 0;           // zero-copy: misses listed for the copy kernel
+    int failed_e = -1;    // the miss whose copy failed, if any
+    cudaError_t failed_ce = cudaSuccess;
     for (int e : miss) {
       const int slot = C->lru.back();  // least recently used; never one touched in pass 1
       C->lru.pop_back();
@@ -363,33 +379,63 @@ int make_resident(k3moe_layer* L, cudaStream_t s) {
       C->lru_pos[slot] = C->lru.begin();
       uint8_t* dst = C->slots + (size_t)slot * C->slot_bytes;
       const bool fake = L->test_fail_copy > 0 && --L->test_fail_copy == 0;  // failure-path test
-      const cudaError_t ce = fake ? cudaErrorInvalidValue
-                                  : cudaMemcpyAsync(dst, L->pool + (size_t)e * L->exp_bytes, L->exp_bytes,
-                                                    cudaMemcpyHostToDevice, C->copy_stream);
+      cudaError_t ce = cudaSuccess;
+      if (fake)
+        ce = cudaErrorInvalidValue;
+      else if (zc)
+        L->miss_host[nm++] = MissCopy{L->pool_dev + (size_t)e * L->exp_bytes, dst};
+      else
+        ce = cudaMemcpyAsync(dst, L->pool + (size_t)e * L->exp_bytes, L->exp_bytes, cudaMemcpyHostToDevice,
+                             C->copy_stream);
       if (ce != cudaSuccess) {
         if (!fake) cudaGetLastError();
         // the slot holds no valid expert: forget it (empty, least recently used) so that no later
-        // call takes it for a hit; the copies issued before it still complete on the copy stream,
-        // and later work on `s` is ordered after them
+        // call takes it for a hit; the copies issued before it still complete, and later work on
+        // `s` is ordered after them
         C->where.erase(key);
         C->slot_key[slot] = -1;
         C->resident[L->uid] -= 1;
         C->lru.erase(C->lru_pos[slot]);
         C->lru.push_back(slot);
         C->lru_pos[slot] = std::prev(C->lru.end());
-        cudaEventRecord(b, C->copy_stream);
-        C->pending.emplace_back(a, b);
-        cudaStreamWaitEvent(s, b, 0);
-        cudaMemcpyAsync((void*)L->eptr_dev, L->eptr_host, (size_t)E * sizeof(void*), cudaMemcpyHostToDevice, s);
-        return fail(K3MOE_ERR_CUDA, "copying expert %d to its cache slot failed: %s", e, cudaGetErrorString(ce));
+        failed_e = e;
+        failed_ce = ce;
+        break;
       }
       L->eptr_host[e] = dst;
       C->st.misses += 1;
       C->st.h2d_bytes += L->exp_bytes;
     }
-    CUDA_TRY(cudaEventRecord(b, C->copy_stream));
-    C->pending.emplace_back(a, b);
-    CUDA_TRY(cudaStreamWaitEvent(s, b, 0));
+    if (zc) {
+      cudaError_t ke = cudaSuccess;
+      if (nm > 0) ke = cudaMemcpyAsync(L->miss_dev, L->miss_host, (size_t)nm * sizeof(MissCopy), cudaMemcpyHostToDevice, s);
+      if (ke == cudaSuccess) ke = launch_miss_copy(L->miss_dev, nm, L->exp_bytes, L->num_sms, s);
+      cudaEventRecord(b, s);
+      C->pending.emplace_back(a, b);
+      if (ke != cudaSuccess) {
+        cudaGetLastError();
+        // none of this call's slots was filled: forget them all
+        for (int i = 0; i < nm; ++i) {
+          const int slot = (int)((L->miss_host[i].dst - C->slots) / C->slot_bytes);
+          C->where.erase(C->slot_key[slot]);
+          C->slot_key[slot] = -1;
+          C->resident[L->uid] -= 1;
+          C->lru.erase(C->lru_pos[slot]);
+          C->lru.push_back(slot);
+          C->lru_pos[slot] = std::prev(C->lru.end());
+        }
+        return fail(K3MOE_ERR_CUDA, "zero-copy miss kernel: %s", cudaGetErrorString(ke));
+      }
+    } else {
+      cudaEventRecord(b, C->copy_stream);
+      C->pending.emplace_back(a, b);
+      cudaStreamWaitEvent(s, b, 0);
+    }
+    if (failed_e >= 0) {
+      cudaMemcpyAsync((void*)L->eptr_dev, L->eptr_host, (size_t)E * sizeof(void*), cudaMemcpyHostToDevice, s);
+      return fail(K3MOE_ERR_CUDA, "copying expert %d to its cache slot failed: %s", failed_e,
+                  cudaGetErrorString(failed_ce));
+    }
   }
   C->st.calls += 1;
   CUDA_TRY(cudaMemcpyAsync((void*)L->eptr_dev, L->eptr_host, (size_t)E * sizeof(void*), cudaMemcpyHostToDevice, s));
@@ -429,6 +475,7 @@ int forward_gemm(k3moe_layer* L, const void* x, int T, float* y, cudaStream_t s)
   q.err = w.sync + 1;
   q.wait_ns = L->wait_ns;
   q.num_sms = L->num_sms;
+  q.act = L->activation;
   rc = timed_launch(L, KID_GATHER, s, [&] {
     cudaError_t e = launch_gemm_prep(q, reinterpret_cast<const uint16_t*>(x), w.counts, w.offsets, D.E, s);
     return e == cudaSuccess ? cudaMemsetAsync(w.hmax, 0, (size_t)P * 4, s) : e;
@@ -440,7 +487,7 @@ int forward_gemm(k3moe_layer* L, const void* x, int T, float* y, cudaStream_t s)
   if (rc) return rc;
   rc = timed_launch(L, KID_GEMM_DN, s, [&] { return launch_gemm_dn(q, s); });
   if (rc) return rc;
-  FfnArgs fa{L->eptr_dev, D.d, D.f, D.E, D.k, T, L->ws, y, L->num_sms, L->wait_ns, 0, 0, 0, nullptr, 0};
+  FfnArgs fa{L->eptr_dev, D.d, D.f, D.E, D.k, T, L->ws, y, L->num_sms, L->wait_ns, 0, 0, 0, nullptr, 0, L->activation};
   return timed_launch(L, KID_COMBINE, s, [&] { return launch_combine(fa, s); });
 }
 
@@ -461,7 +508,7 @@ int forward_impl(k3moe_layer* L, const void* x, int T, float* y, cudaStream_t s)
     if (rc) return rc;
   }
   FfnArgs fa{L->eptr_dev, D.d, D.f, D.E, D.k, T, L->ws, y, L->num_sms, L->wait_ns, L->test_stall, L->ring_depth,
-             L->zero_scales ? 1 : 0, L->cache ? nullptr : L->packed, L->exp_bytes};
+             L->zero_scales ? 1 : 0, L->cache ? nullptr : L->packed, L->exp_bytes, L->activation};
   L->test_stall = 0;
   rc = timed_launch(L, KID_GATEUP, s, [&] { return launch_gateup(fa, s); });
   if (rc) return rc;
@@ -632,7 +679,10 @@ int k3moe_pack_experts(const k3moe_dims* dims, const void* canon_nib, const void
       return bail(fail(K3MOE_ERR_OOM, "packed experts: cudaMalloc(%zu) failed", (size_t)D.E * eb));
     }
   } else {
-    if (cudaHostAlloc(&L->pool, (size_t)D.E * eb, cudaHostAllocDefault) != cudaSuccess ||
+    if (cudaHostAlloc(&L->pool, (size_t)D.E * eb, cudaHostAllocMapped) != cudaSuccess ||
+        cudaHostGetDevicePointer((void**)&L->pool_dev, L->pool, 0) != cudaSuccess ||
+        cudaHostAlloc((void**)&L->miss_host, (size_t)D.E * sizeof(MissCopy), cudaHostAllocDefault) != cudaSuccess ||
+        cudaMalloc((void**)&L->miss_dev, (size_t)D.E * sizeof(MissCopy)) != cudaSuccess ||
         cudaHostAlloc((void**)&L->eptr_host, (size_t)D.E * sizeof(void*), cudaHostAllocDefault) != cudaSuccess ||
         cudaHostAlloc((void**)&L->act_host, (size_t)(D.E + 1) * 4, cudaHostAllocDefault) != cudaSuccess ||
         cudaMalloc(&stage_out, (size_t)chunk * eb) != cudaSuccess) {
@@ -824,6 +874,16 @@ int k3moe_set_option(k3moe_layer* L, int option, long long value) {
       if (value != K3MOE_PATH_AUTO && value != K3MOE_PATH_DECODE && value != K3MOE_PATH_GEMM)
         return fail(K3MOE_ERR_INVALID_ARG, "unknown path %lld", value);
       L->path = (int)value;
+      return K3MOE_OK;
+    case K3MOE_OPT_MISS_PATH:
+      if (value != K3MOE_MISS_COPY_ENGINE && value != K3MOE_MISS_ZERO_COPY)
+        return fail(K3MOE_ERR_INVALID_ARG, "unknown miss path %lld", value);
+      L->miss_path = (int)value;
+      return K3MOE_OK;
+    case K3MOE_OPT_ACTIVATION:
+      if (value != K3MOE_ACT_SWIGLU && value != K3MOE_ACT_SITU_GLU)
+        return fail(K3MOE_ERR_INVALID_ARG, "unknown activation %lld", value);
+      L->activation = (int)value;
       return K3MOE_OK;
     case K3MOE_OPT_GEMM_MIN_T:
       if (value < 1) return fail(K3MOE_ERR_INVALID_ARG, "GEMM_MIN_T must be >= 1");

@@ -19,8 +19,8 @@
 //   gateup_kernel  task = (unit, 16 rows of f); stage = one 128-column k-tile of the gate and
 //                  up tiles (2176 B) + the unit's x fragments for it; consumer warp w takes
 //                  k-tiles kt % 8 == w; one of 2 epilogue warps adds the 8 partial sums in
-//                  warp order, applies SwiGLU h = silu(g) * u, writes h (fp32) and records
-//                  max |h| per pick.
+//                  warp order, applies SwiGLU h = silu(g) * u (or SiTU-GLU, gate_act), writes
+//                  h (fp32) and records max |h| per pick.
 //   hconv_kernel   h -> fp16 B fragments with one power-of-two scale per pick (fp16 never
 //                  overflows; the scale factors out of the down projection's sum).
 //   down_kernel    task = (unit, 32 rows of d) over the whole f range, streamed in chunks of
@@ -459,7 +459,7 @@ __global__ void __launch_bounds__(kGuThreads, 2) gateup_kernel(FfnArgs a, GuLayo
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const float gv = v[0 * 4 + 2 * h + c] * xs, uv = v[1 * 4 + 2 * h + c] * xs;
-            const float hv = gv / (1.0f + expf(-gv)) * uv;
+            const float hv = gate_act(gv, a.act) * uv;
             a.ws.hbuf[(size_t)p * a.f + rg * kTileRows + g + 8 * h] = hv;
             hmx[c] = fmaxf(hmx[c], fabsf(hv));
           }

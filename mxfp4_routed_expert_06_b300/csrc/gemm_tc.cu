@@ -248,6 +248,7 @@ struct GemmArgs {
   float* obuf;              // DN output [P][d] by pick
   uint32_t* err;
   unsigned long long wait_ns;
+  int act;                  // gate activation (K3MOE_ACT_*), mode 0
 };
 
 // Raw bytes one decoder lane needs for one stage: two tile halves (16 nibble bytes each) and
@@ -376,7 +377,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const float g = __uint_as_float(gr[j]) * sc, u = __uint_as_float(ur[j]) * sc;
-              const float hv = g / (1.0f + expf(-g)) * u;
+              const float hv = gate_act(g, a.act) * u;
               gr[j] = __float_as_uint(hv);
               mx = fmaxf(mx, fabsf(hv));
             }
@@ -768,6 +769,7 @@ GemmArgs common_args(const GemmFfn& q, int mode) {
   g.wgt = q.w;
   g.err = q.err;
   g.wait_ns = q.wait_ns;
+  g.act = q.act;
   return g;
 }
 }  // namespace

@@ -176,6 +176,15 @@ inline cudaError_t set_smem_limit_once(Fn* kernel, int bytes, std::atomic<unsign
   return e;
 }
 
+// Gate activation of the expert FFN, h = gate_act(g) * u (K3MOE_ACT_*).  SwiGLU keeps the exact
+// expression silu(g) = g / (1 + exp(-g)); SiTU-GLU is beta1 * beta2 * sigmoid(g) * tanh(g / beta2)
+// with beta1 = 4, beta2 = 25 (the pages' parameters; the formula is a reading of their glossary).
+constexpr float kSituBeta1 = 4.0f, kSituBeta2 = 25.0f;
+__device__ __forceinline__ float gate_act(float g, int act) {
+  if (act == K3MOE_ACT_SITU_GLU) return kSituBeta1 * kSituBeta2 * (1.0f / (1.0f + expf(-g))) * tanhf(g / kSituBeta2);
+  return g / (1.0f + expf(-g));
+}
+
 // Device error flags (ws.sync[1]).
 constexpr uint32_t kErrTimeout = 1u;
 constexpr uint32_t kErrBadAccess = 2u;  // self-checking builds only: a copy address failed its check
@@ -192,6 +201,7 @@ struct FfnArgs {
   int zero_scales;                   // 1: some E8M0 scale byte is 0 (exact subnormal decode needed)
   const uint8_t* expert_base;        // non-null: expert e is at expert_base + e * expert_stride (no
   size_t expert_stride;              //   table lookup); null: expert_ptr[e] (device cache mode)
+  int act;                           // gate activation (K3MOE_ACT_*)
 };
 cudaError_t launch_gateup(const FfnArgs& a, cudaStream_t s);
 cudaError_t launch_down(const FfnArgs& a, cudaStream_t s);
@@ -217,6 +227,7 @@ struct GemmFfn {
   uint32_t* err;
   unsigned long long wait_ns;
   int num_sms;
+  int act;                   // gate activation (K3MOE_ACT_*)
 };
 bool gemm_scales_ok(int s_min, int s_max);
 cudaError_t launch_gemm_prep(const GemmFfn& q, const uint16_t* x, const int32_t* counts, const int32_t* offsets,
@@ -231,6 +242,14 @@ cudaError_t launch_router_tc(const uint16_t* x, int T, int d, int E, const uint1
 cudaError_t launch_split_router(const float* W, int E, int d, uint16_t* out, cudaStream_t s);
 cudaError_t launch_residual_rmsnorm(const float* y, const uint16_t* x, int T, int d, float eps, uint16_t* x_next,
                                     uint16_t* x_norm, cudaStream_t s);
+
+// Zero-copy miss path of the expert cache: copy n experts of `bytes` each from the mapped pinned
+// pool (device view) into their slots, in one launch on `s`.
+struct MissCopy {
+  const uint8_t* src;  // device address of the expert in the mapped pinned pool
+  uint8_t* dst;        // its device slot
+};
+cudaError_t launch_miss_copy(const MissCopy* list, int n, size_t bytes, int num_sms, cudaStream_t s);
 
 // canon_nib/canon_scl point at the canonical bytes of the first of n_exp experts; dst at its packed block.
 cudaError_t launch_pack(const uint8_t* canon_nib, const uint8_t* canon_scl, int n_exp, int d, int f, uint8_t* dst,

@@ -348,3 +348,23 @@ def test_zero_scale_bytes():
     L = Small(d, f, E, k, 6, seed=3, nib=nib, scl=scl)
     _check_layer(L, L.tokens(6), "zero scales")
     L.free()
+
+
+@pytest.mark.parametrize("path,T", [("decode", 5), ("decode", 40), ("gemm", 300)])
+def test_situ_glu_option_matches_oracle(path, T):
+    # K3MOE_OPT_ACTIVATION = SiTU-GLU (a reading of the deep dive's glossary entry; the oracle
+    # restates the same reading): both FFN paths against the oracle, and the option takes effect.
+    d, f, E, k = 512, 256, 16, 4
+    L = Small(d, f, E, k, T, seed=77 + T)
+    x = L.tokens(T)
+    k3.k3moe_set_option(L.layer, k3.K3MOE_OPT_PATH, k3.K3MOE_PATH_GEMM if path == "gemm" else k3.K3MOE_PATH_DECODE)
+    y_swiglu = L.forward(x)
+    k3.k3moe_set_option(L.layer, k3.K3MOE_OPT_ACTIVATION, k3.K3MOE_ACT_SITU_GLU)
+    y = L.forward(x)
+    ref = oracle.layer(x, L.Wr, None, k, f, L.nib, L.scl, act=oracle.ACT_SITU_GLU)
+    assert_y_close(y, ref["y"], ref["sumabs"], f"SiTU-GLU, {path} path, T={T}")
+    assert not np.allclose(y, y_swiglu)
+    assert np.array_equal(L.forward(x), y)  # deterministic
+    with pytest.raises(k3.K3MoEError):
+        k3.k3moe_set_option(L.layer, k3.K3MOE_OPT_ACTIVATION, 7)
+    L.free()
