@@ -432,6 +432,8 @@ def run_stack4(args):
         synth.experts_to_device(SEED, l, 0, E, D, F, dn.data_ptr(), ds.data_ptr())
         Wr = torch.from_numpy(synth.router_weights(SEED, l, E, D)).cuda()
         layers.append(k3.k3moe_pack_experts(k3.dims(D, F, E, K, 1), dn, ds, 1, Wr, None, cache))
+        k3.k3moe_set_option(layers[-1], k3.K3MOE_OPT_MISS_PATH,
+                            k3.K3MOE_MISS_ZERO_COPY if args.miss_path == "zero-copy" else k3.K3MOE_MISS_COPY_ENGINE)
         del dn, ds, Wr
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
@@ -527,6 +529,7 @@ def run_stack4(args):
             "data": "synthetic (seeded splitmix64 experts, N(0,1) bf16 tokens, N(0,1/d) router)",
             "impl": "b300",
             "config": {"workload": WORKLOADS["stack4"]["desc"], "budget_gb": args.budget_gb,
+                       "miss_path": args.miss_path,
                        "cache_slots": budget // EXPERT_BYTES, "tokens_per_step": n_tok, "layers": n_layers,
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                        "l2": "inputs larger than L2: 62.9 GB pool"},
@@ -689,6 +692,8 @@ def main():
                     help="tokens per step of the decode workloads: T=1 calls (default 1000; 256 for stack4); "
                          "the T=64 workload runs this many tokens in T=64 calls")
     ap.add_argument("--budget-gb", type=float, default=8.0, help="stack4: device cache budget (1 GB = 1e9 B)")
+    ap.add_argument("--miss-path", default="copy-engine", choices=["copy-engine", "zero-copy"],
+                    help="stack4: how missed experts reach their slots (K3MOE_OPT_MISS_PATH)")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--experts", type=int, default=E,

@@ -147,12 +147,13 @@ def test_small_stack_budgets_bit_identical():
         k3.k3moe_cache_destroy(c)
 
 
-@pytest.mark.parametrize("fail_at,slots", [(1, 64), (3, 64), (6, 10)])
-def test_failed_expert_copy_reports_error_then_recovers(fail_at, slots):
+@pytest.mark.parametrize("fail_at,slots,miss_path", [(1, 64, 0), (3, 64, 0), (6, 10, 0), (1, 64, 1), (6, 10, 1)])
+def test_failed_expert_copy_reports_error_then_recovers(fail_at, slots, miss_path):
     """A cache-miss copy that fails (injected on the host: the copy call reports an error and
     copies nothing) makes that forward return K3MOE_ERR_CUDA; the slot it was filling is
     forgotten, so the following calls copy the expert again and give the device-resident
-    output, byte for byte."""
+    output, byte for byte.  miss_path 1: the zero-copy miss path (the misses listed before the
+    failing one are still copied by the kernel)."""
     d, f, E, k, T, steps = 512, 256, 32, 4, 2, 6
     dm = k3.dims(d, f, E, k, T)
     eb = k3.k3moe_packed_expert_bytes(dm)
@@ -162,6 +163,7 @@ def test_failed_expert_copy_reports_error_then_recovers(fail_at, slots):
     ref_layer = k3.k3moe_pack_experts(dm, nib, scl, 0, Wr)
     cache = k3.k3moe_cache_create(slots * eb, eb)
     layer = k3.k3moe_pack_experts(dm, nib, scl, 0, Wr, None, cache)
+    k3.k3moe_set_option(layer, k3.K3MOE_OPT_MISS_PATH, miss_path)
     try:
         refs = []
         for x in xs:
@@ -188,6 +190,38 @@ def test_failed_expert_copy_reports_error_then_recovers(fail_at, slots):
         k3.k3moe_layer_free(layer)
         k3.k3moe_layer_free(ref_layer)
         k3.k3moe_cache_destroy(cache)
+
+
+def test_zero_copy_miss_path_matches_copy_engine():
+    """Two stacked layers sharing a cache that holds about half their experts: the zero-copy miss
+    path (one kernel per call reads the misses from the mapped pinned pool) gives the same bytes
+    as the device-resident layers, and the same hits, misses and evictions as the copy-engine
+    path (the bookkeeping is shared; only how the bytes travel differs)."""
+    d, f, E, k, T, n_layers, steps = 512, 256, 32, 4, 3, 2, 16
+    dm = k3.dims(d, f, E, k, T)
+    eb = k3.k3moe_packed_expert_bytes(dm)
+    host = [synth.experts(15, l, 0, E, d, f) for l in range(n_layers)]
+    Wr = [synth.router_weights(15, l, E, d) for l in range(n_layers)]
+    x0 = [torch.from_numpy(synth.tokens_bf16(15, 0, s * T, T, d).view(np.int16)).cuda() for s in range(steps)]
+    dev = [k3.k3moe_pack_experts(dm, host[l][0], host[l][1], 0, Wr[l]) for l in range(n_layers)]
+    y_ref, _ = _run_stack(dev, x0, T, steps, d)
+    stats = {}
+    for miss_path in (k3.K3MOE_MISS_COPY_ENGINE, k3.K3MOE_MISS_ZERO_COPY):
+        cache = k3.k3moe_cache_create(E * eb, eb)
+        layers = [k3.k3moe_pack_experts(dm, host[l][0], host[l][1], 0, Wr[l], None, cache) for l in range(n_layers)]
+        for L in layers:
+            k3.k3moe_set_option(L, k3.K3MOE_OPT_MISS_PATH, miss_path)
+        y, _ = _run_stack(layers, x0, T, steps, d)
+        assert np.array_equal(y, y_ref), f"miss path {miss_path}: y differs from the device-resident layers"
+        st = k3.k3moe_cache_stats(cache)
+        assert st["misses"] > 0 and st["evictions"] > 0 and st["h2d_bytes"] == st["misses"] * eb
+        stats[miss_path] = (st["hits"], st["misses"], st["evictions"])
+        for L in layers:
+            k3.k3moe_layer_free(L)
+        k3.k3moe_cache_destroy(cache)
+    assert stats[k3.K3MOE_MISS_COPY_ENGINE] == stats[k3.K3MOE_MISS_ZERO_COPY]
+    for L in dev:
+        k3.k3moe_layer_free(L)
 
 
 def test_budget_too_small_then_recovers():
