@@ -100,6 +100,37 @@ size_t k3moe_packed_expert_bytes(const k3moe_dims* dims);
 int k3moe_pack_experts(const k3moe_dims* dims, const void* canon_nib, const void* canon_scale, int src_on_device,
                        const float* W_r, const float* bias, k3moe_cache* cache, void* stream, k3moe_layer** out);
 
+/* Packed-pool header.  It describes a packed expert pool (the bytes k3moe_read_packed returns,
+ * experts 0..E-1 back to back) so that a saved pool can be validated and loaded again with
+ * k3moe_layer_from_packed, without repacking from the canonical layout.  The pages' engine
+ * streams a prepacked trunk ("one layer = one read"); this is the expert-pool counterpart. */
+#define K3MOE_POOL_MAGIC 0x584D334Bu /* the bytes "K3MX" */
+#define K3MOE_POOL_VERSION 1         /* the 16 x 128 tile layout this library writes */
+typedef struct {
+  uint32_t magic;         /* K3MOE_POOL_MAGIC */
+  uint32_t version;       /* K3MOE_POOL_VERSION */
+  int32_t d, f, E;        /* dimensions of the experts and their count */
+  int32_t s_min, s_max;   /* smallest and largest E8M0 scale byte in the pool */
+  int32_t zero_scales;    /* 1 when some scale byte is 0 (then s_min is 0) */
+  uint64_t expert_bytes;  /* packed bytes per expert (k3moe_packed_expert_bytes) */
+  uint64_t checksum;      /* FNV-1a 64 of every byte of the header before this field */
+} k3moe_pool_header;
+
+/* Fill `out` for the layer's packed pool.  Errors: INVALID_ARG (NULL). */
+int k3moe_pool_header_get(k3moe_layer* layer, k3moe_pool_header* out);
+/* 0 when `header` describes a pool this library can load for `dims` (magic, version, checksum,
+ * d, f, E, expert size, a valid scale range), else INVALID_ARG with the mismatch in the message.
+ * Host only. */
+int k3moe_pool_header_check(const k3moe_pool_header* header, const k3moe_dims* dims);
+/* Build a layer from a packed pool (as saved from k3moe_read_packed, with its header) instead of
+ * canonical bytes; otherwise as k3moe_pack_experts (router, bias, cache and stream arguments, and
+ * ownership).  packed: E * header->expert_bytes bytes, host or device per src_on_device.  The pool
+ * is copied as is (it is trusted to match the header; the header is checked first).  Errors:
+ * INVALID_ARG (a header that fails k3moe_pool_header_check, NULL pointers), OOM, CUDA. */
+int k3moe_layer_from_packed(const k3moe_dims* dims, const k3moe_pool_header* header, const void* packed,
+                            int src_on_device, const float* W_r, const float* bias, k3moe_cache* cache, void* stream,
+                            k3moe_layer** out);
+
 /* Router alone ("what you learn", router paragraph; invariants row 5):
  *   logit[t,e] = sum_j x[t,j]*W_r[e,j] (fp32 accumulate), sigma = 1/(1+exp(-logit)),
  *   key = sigma + bias[e]; idx[t,:] = the k experts with the largest keys in descending key

@@ -30,8 +30,8 @@ _lib = ctypes.CDLL(LIB_PATH)
 def _header_constants() -> dict:
     out = {}
     with open(HEADER) as fh:
-        for m in re.finditer(r"#define\s+(K3MOE_\w+)\s+\(?(-?\d+)\)?", fh.read()):
-            out[m.group(1)] = int(m.group(2))
+        for m in re.finditer(r"#define\s+(K3MOE_\w+)\s+\(?(-?(?:0x[0-9A-Fa-f]+|\d+))u?\)?", fh.read()):
+            out[m.group(1)] = int(m.group(2), 0)
     return out
 
 
@@ -53,6 +53,12 @@ class k3moe_cache_stats_t(ctypes.Structure):
 
 class k3moe_cache_sim_stats(ctypes.Structure):
     _fields_ = [("hits", ctypes.c_longlong), ("misses", ctypes.c_longlong), ("evictions", ctypes.c_longlong)]
+
+
+class k3moe_pool_header(ctypes.Structure):
+    _fields_ = [("magic", ctypes.c_uint32), ("version", ctypes.c_uint32), ("d", ctypes.c_int32),
+                ("f", ctypes.c_int32), ("E", ctypes.c_int32), ("s_min", ctypes.c_int32), ("s_max", ctypes.c_int32),
+                ("zero_scales", ctypes.c_int32), ("expert_bytes", ctypes.c_uint64), ("checksum", ctypes.c_uint64)]
 
 
 class k3moe_kernel_time(ctypes.Structure):
@@ -83,6 +89,10 @@ _SIGS = {
     "k3moe_cache_simulate": ([_vp, _vp, _i, _i, _i, ctypes.c_ulonglong, ctypes.POINTER(k3moe_cache_sim_stats)], _i),
     "k3moe_last_error": ([], ctypes.c_char_p),
     "k3moe_router_topk_noalloc": ([_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp], _i),
+    "k3moe_pool_header_get": ([_vp, ctypes.POINTER(k3moe_pool_header)], _i),
+    "k3moe_pool_header_check": ([ctypes.POINTER(k3moe_pool_header), ctypes.POINTER(k3moe_dims)], _i),
+    "k3moe_layer_from_packed": ([ctypes.POINTER(k3moe_dims), ctypes.POINTER(k3moe_pool_header), _vp, _i, _vp, _vp,
+                                 _vp, _vp, ctypes.POINTER(_vp)], _i),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -152,6 +162,24 @@ def k3moe_pack_experts(dm: k3moe_dims, canon_nib, canon_scale, src_on_device: in
     out = ctypes.c_void_p()
     _check(_lib.k3moe_pack_experts(ctypes.byref(dm), _ptr(canon_nib), _ptr(canon_scale), int(src_on_device),
                                    _ptr(W_r), _ptr(bias), _handle(cache), _stream(stream), ctypes.byref(out)))
+    return out
+
+
+def k3moe_pool_header_get(layer) -> k3moe_pool_header:
+    h = k3moe_pool_header()
+    _check(_lib.k3moe_pool_header_get(_handle(layer), ctypes.byref(h)))
+    return h
+
+
+def k3moe_pool_header_check(header: k3moe_pool_header, dm: k3moe_dims) -> None:
+    _check(_lib.k3moe_pool_header_check(ctypes.byref(header), ctypes.byref(dm)))
+
+
+def k3moe_layer_from_packed(dm: k3moe_dims, header: k3moe_pool_header, packed, src_on_device: int, W_r, bias=None,
+                            cache=None, stream=None):
+    out = ctypes.c_void_p()
+    _check(_lib.k3moe_layer_from_packed(ctypes.byref(dm), ctypes.byref(header), _ptr(packed), int(src_on_device),
+                                        _ptr(W_r), _ptr(bias), _handle(cache), _stream(stream), ctypes.byref(out)))
     return out
 
 

@@ -1,6 +1,7 @@
 // capi.cu -- the C ABI (include/k3moe.h): argument checks, ownership, workspace, dispatch,
 // and the expert cache's host-side LRU bookkeeping.
 #include <cstdarg>
+#include <cstddef>
 #include <cstdio>
 #include <cstring>
 #include <iterator>
@@ -609,19 +610,24 @@ void k3moe_cache_destroy(k3moe_cache* C) {
   delete C;
 }
 
-int k3moe_pack_experts(const k3moe_dims* dims, const void* canon_nib, const void* canon_scale, int src_on_device,
-                       const float* W_r, const float* bias, k3moe_cache* cache, void* stream, k3moe_layer** out) {
-  if (!out) return fail(K3MOE_ERR_INVALID_ARG, "out is NULL");
+}  // extern "C"
+
+namespace {
+
+// A layer with everything but its expert bytes: workspace, router (and its bf16 split), pointer
+// table, and the storage the experts will fill (the device block, or in cache mode the mapped
+// pinned pool and its host-side tables).  On failure nothing is left allocated.
+int layer_begin(const k3moe_dims* dims, int src_on_device, const float* W_r, const float* bias, k3moe_cache* cache,
+                cudaStream_t s, k3moe_layer** out) {
   *out = nullptr;
   int rc = check_dims(dims);
   if (rc) return rc;
-  if (!canon_nib || !canon_scale || !W_r) return fail(K3MOE_ERR_INVALID_ARG, "NULL input pointer");
+  if (!W_r) return fail(K3MOE_ERR_INVALID_ARG, "NULL input pointer");
   if (src_on_device != 0 && src_on_device != 1) return fail(K3MOE_ERR_INVALID_ARG, "src_on_device must be 0 or 1");
   const k3moe_dims D = *dims;
   const size_t eb = packed_expert_bytes(D.d, D.f);
   if (cache && cache->slot_bytes != eb)
     return fail(K3MOE_ERR_INVALID_ARG, "cache slot_bytes %zu != packed expert bytes %zu", cache->slot_bytes, eb);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   k3moe_layer* L = new k3moe_layer();
   L->dims = D;
   L->exp_bytes = eb;
@@ -634,6 +640,7 @@ int k3moe_pack_experts(const k3moe_dims* dims, const void* canon_nib, const void
     cudaGetLastError();
   }
   auto bail = [&](int code) {
+    L->cache = nullptr;  // not attached yet
     free_layer(L);
     return code;
   };
@@ -655,27 +662,9 @@ int k3moe_pack_experts(const k3moe_dims* dims, const void* canon_nib, const void
   }
   if (launch_split_router(L->Wr, D.E, D.d, L->Wsplit, s) != cudaSuccess)
     return bail(fail(K3MOE_ERR_CUDA, "router split failed: %s", cudaGetErrorString(cudaGetLastError())));
-
-  const size_t cn = 3ull * D.f * D.d / 2, cs = 3ull * D.f * D.d / 32;
-  // chunk of experts packed per pass: bounded staging (about 2 GB)
-  int chunk = (int)std::max<size_t>(1, std::min<size_t>(D.E, (size_t)(2ull << 30) / (cn + cs + eb)));
-  uint8_t* stage_nib = nullptr;
-  uint8_t* stage_scl = nullptr;
-  uint8_t* stage_out = nullptr;
-  if (!src_on_device) {
-    if (cudaMalloc(&stage_nib, (size_t)chunk * cn) != cudaSuccess ||
-        cudaMalloc(&stage_scl, (size_t)chunk * cs) != cudaSuccess) {
-      cudaGetLastError();
-      cudaFree(stage_nib);
-      return bail(fail(K3MOE_ERR_OOM, "pack staging allocation failed"));
-    }
-  }
-  bool ok = true;
   if (!cache) {
     if (cudaMalloc(&L->packed, (size_t)D.E * eb) != cudaSuccess) {
       cudaGetLastError();
-      cudaFree(stage_nib);
-      cudaFree(stage_scl);
       return bail(fail(K3MOE_ERR_OOM, "packed experts: cudaMalloc(%zu) failed", (size_t)D.E * eb));
     }
   } else {
@@ -684,16 +673,77 @@ int k3moe_pack_experts(const k3moe_dims* dims, const void* canon_nib, const void
         cudaHostAlloc((void**)&L->miss_host, (size_t)D.E * sizeof(MissCopy), cudaHostAllocDefault) != cudaSuccess ||
         cudaMalloc((void**)&L->miss_dev, (size_t)D.E * sizeof(MissCopy)) != cudaSuccess ||
         cudaHostAlloc((void**)&L->eptr_host, (size_t)D.E * sizeof(void*), cudaHostAllocDefault) != cudaSuccess ||
-        cudaHostAlloc((void**)&L->act_host, (size_t)(D.E + 1) * 4, cudaHostAllocDefault) != cudaSuccess ||
-        cudaMalloc(&stage_out, (size_t)chunk * eb) != cudaSuccess) {
+        cudaHostAlloc((void**)&L->act_host, (size_t)(D.E + 1) * 4, cudaHostAllocDefault) != cudaSuccess) {
       cudaGetLastError();
-      cudaFree(stage_nib);
-      cudaFree(stage_scl);
-      cudaFree(stage_out);
       return bail(fail(K3MOE_ERR_OOM, "pinned expert pool of %zu bytes could not be allocated", (size_t)D.E * eb));
     }
     memset((void*)L->eptr_host, 0, (size_t)D.E * sizeof(void*));
   }
+  *out = L;
+  return K3MOE_OK;
+}
+
+// The experts are in place: fill the device pointer table (device mode) or attach to the cache.
+int layer_finish(k3moe_layer* L, cudaStream_t s) {
+  const k3moe_dims& D = L->dims;
+  if (!L->cache) {
+    std::vector<const uint8_t*> ptrs(D.E);
+    for (int e = 0; e < D.E; ++e) ptrs[e] = L->packed + (size_t)e * L->exp_bytes;
+    if (cudaMemcpy((void*)L->eptr_dev, ptrs.data(), (size_t)D.E * sizeof(void*), cudaMemcpyHostToDevice) !=
+        cudaSuccess)
+      return fail(K3MOE_ERR_CUDA, "pointer table upload failed");
+  } else {
+    k3moe_cache* C = L->cache;
+    L->cache = nullptr;
+    attach_cache(L, C);
+  }
+  L->last_stream = s;
+  return K3MOE_OK;
+}
+
+uint64_t pool_header_checksum(const k3moe_pool_header* h) {  // FNV-1a 64 over every field before it
+  const uint8_t* p = reinterpret_cast<const uint8_t*>(h);
+  uint64_t x = 1469598103934665603ull;
+  for (size_t i = 0; i < offsetof(k3moe_pool_header, checksum); ++i) x = (x ^ p[i]) * 1099511628211ull;
+  return x;
+}
+
+}  // namespace
+
+extern "C" {
+
+int k3moe_pack_experts(const k3moe_dims* dims, const void* canon_nib, const void* canon_scale, int src_on_device,
+                       const float* W_r, const float* bias, k3moe_cache* cache, void* stream, k3moe_layer** out) {
+  if (!out) return fail(K3MOE_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!canon_nib || !canon_scale) return fail(K3MOE_ERR_INVALID_ARG, "NULL input pointer");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  k3moe_layer* L = nullptr;
+  int rc = layer_begin(dims, src_on_device, W_r, bias, cache, s, &L);
+  if (rc) return rc;
+  const k3moe_dims D = *dims;
+  const size_t eb = L->exp_bytes;
+  auto bail = [&](int code) {
+    L->cache = nullptr;
+    free_layer(L);
+    return code;
+  };
+  const size_t cn = 3ull * D.f * D.d / 2, cs = 3ull * D.f * D.d / 32;
+  // chunk of experts packed per pass: bounded staging (about 2 GB)
+  int chunk = (int)std::max<size_t>(1, std::min<size_t>(D.E, (size_t)(2ull << 30) / (cn + cs + eb)));
+  uint8_t* stage_nib = nullptr;
+  uint8_t* stage_scl = nullptr;
+  uint8_t* stage_out = nullptr;
+  if ((!src_on_device && (cudaMalloc(&stage_nib, (size_t)chunk * cn) != cudaSuccess ||
+                          cudaMalloc(&stage_scl, (size_t)chunk * cs) != cudaSuccess)) ||
+      (cache && cudaMalloc(&stage_out, (size_t)chunk * eb) != cudaSuccess)) {
+    cudaGetLastError();
+    cudaFree(stage_nib);
+    cudaFree(stage_scl);
+    cudaFree(stage_out);
+    return bail(fail(K3MOE_ERR_OOM, "pack staging allocation failed"));
+  }
+  bool ok = true;
   {
     const int32_t init[4] = {0, 255, 0, 0};  // flags, min scale byte, max scale byte
     ok = cudaMemcpyAsync(L->ws.bad, init, sizeof(init), cudaMemcpyHostToDevice, s) == cudaSuccess &&
@@ -719,7 +769,7 @@ int k3moe_pack_experts(const k3moe_dims* dims, const void* canon_nib, const void
     if (ok && cache)
       ok = cudaMemcpyAsync(L->pool + (size_t)e0 * eb, stage_out, (size_t)n * eb, cudaMemcpyDeviceToHost, s) ==
            cudaSuccess;
-    if (ok && !src_on_device) ok = cudaStreamSynchronize(s) == cudaSuccess;  // staging reused next chunk
+    if (ok && (!src_on_device || cache)) ok = cudaStreamSynchronize(s) == cudaSuccess;  // staging reused next chunk
   }
   int32_t flags[4] = {0, 255, 0, 0};
   if (ok) ok = cudaMemcpyAsync(flags, L->ws.bad, sizeof(flags), cudaMemcpyDeviceToHost, s) == cudaSuccess;
@@ -733,16 +783,81 @@ int k3moe_pack_experts(const k3moe_dims* dims, const void* canon_nib, const void
   L->zero_scales = (bad & 2) != 0;
   L->s_min = flags[1];
   L->s_max = flags[2];
-  if (!cache) {
-    std::vector<const uint8_t*> ptrs(D.E);
-    for (int e = 0; e < D.E; ++e) ptrs[e] = L->packed + (size_t)e * eb;
-    if (cudaMemcpy((void*)L->eptr_dev, ptrs.data(), (size_t)D.E * sizeof(void*), cudaMemcpyHostToDevice) !=
-        cudaSuccess)
-      return bail(fail(K3MOE_ERR_CUDA, "pointer table upload failed"));
-  } else {
-    attach_cache(L, cache);
+  if ((rc = layer_finish(L, s))) return bail(rc);
+  *out = L;
+  return K3MOE_OK;
+}
+
+int k3moe_pool_header_get(k3moe_layer* L, k3moe_pool_header* out) {
+  if (!L || !out) return fail(K3MOE_ERR_INVALID_ARG, "NULL argument");
+  memset(out, 0, sizeof(*out));
+  out->magic = K3MOE_POOL_MAGIC;
+  out->version = K3MOE_POOL_VERSION;
+  out->d = L->dims.d;
+  out->f = L->dims.f;
+  out->E = L->dims.E;
+  out->s_min = L->s_min;
+  out->s_max = L->s_max;
+  out->zero_scales = L->zero_scales ? 1 : 0;
+  out->expert_bytes = L->exp_bytes;
+  out->checksum = pool_header_checksum(out);
+  return K3MOE_OK;
+}
+
+int k3moe_pool_header_check(const k3moe_pool_header* h, const k3moe_dims* dims) {
+  if (!h || !dims) return fail(K3MOE_ERR_INVALID_ARG, "NULL argument");
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if (h->magic != K3MOE_POOL_MAGIC) return fail(K3MOE_ERR_INVALID_ARG, "not a packed-pool header (magic 0x%08x)", h->magic);
+  if (h->version != K3MOE_POOL_VERSION)
+    return fail(K3MOE_ERR_INVALID_ARG, "packed-pool layout version %u, this library writes %u", h->version,
+                (unsigned)K3MOE_POOL_VERSION);
+  if (h->checksum != pool_header_checksum(h)) return fail(K3MOE_ERR_INVALID_ARG, "packed-pool header checksum mismatch");
+  if (h->d != dims->d || h->f != dims->f || h->E != dims->E)
+    return fail(K3MOE_ERR_INVALID_ARG, "pool holds d=%d f=%d E=%d, dims say d=%d f=%d E=%d", h->d, h->f, h->E, dims->d,
+                dims->f, dims->E);
+  if (h->expert_bytes != packed_expert_bytes(dims->d, dims->f))
+    return fail(K3MOE_ERR_INVALID_ARG, "pool expert size %llu != %zu", (unsigned long long)h->expert_bytes,
+                packed_expert_bytes(dims->d, dims->f));
+  if (h->s_min < 0 || h->s_max > 254 || h->s_min > h->s_max || (h->zero_scales != 0 && h->zero_scales != 1) ||
+      (h->zero_scales == 1) != (h->s_min == 0))
+    return fail(K3MOE_ERR_INVALID_ARG, "pool scale range %d..%d (zero flag %d) is not valid", h->s_min, h->s_max,
+                h->zero_scales);
+  return K3MOE_OK;
+}
+
+int k3moe_layer_from_packed(const k3moe_dims* dims, const k3moe_pool_header* header, const void* packed,
+                            int src_on_device, const float* W_r, const float* bias, k3moe_cache* cache, void* stream,
+                            k3moe_layer** out) {
+  if (!out) return fail(K3MOE_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!packed) return fail(K3MOE_ERR_INVALID_ARG, "NULL input pointer");
+  int rc = k3moe_pool_header_check(header, dims);
+  if (rc) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  k3moe_layer* L = nullptr;
+  if ((rc = layer_begin(dims, src_on_device, W_r, bias, cache, s, &L))) return rc;
+  const size_t total = (size_t)dims->E * L->exp_bytes;
+  cudaError_t e;
+  if (!cache)
+    e = cudaMemcpyAsync(L->packed, packed, total, src_on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, s);
+  else
+    e = cudaMemcpyAsync(L->pool, packed, total, src_on_device ? cudaMemcpyDeviceToHost : cudaMemcpyHostToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    L->cache = nullptr;
+    free_layer(L);
+    return fail(K3MOE_ERR_CUDA, "packed pool copy failed: %s", cudaGetErrorString(e));
   }
-  L->last_stream = s;
+  L->s_min = header->s_min;
+  L->s_max = header->s_max;
+  L->zero_scales = header->zero_scales != 0;
+  if ((rc = layer_finish(L, s))) {
+    L->cache = nullptr;
+    free_layer(L);
+    return rc;
+  }
   *out = L;
   return K3MOE_OK;
 }

@@ -85,3 +85,40 @@ def test_bad_arguments_are_refused_without_device_work():
 def test_free_null_is_harmless():
     k3.k3moe_layer_free(None)
     k3.k3moe_cache_destroy(None)
+
+
+def _fnv1a64(b: bytes) -> int:
+    x = 1469598103934665603
+    for c in b:
+        x = ((x ^ c) * 1099511628211) & 0xFFFFFFFFFFFFFFFF
+    return x
+
+
+def _header(**kw):
+    import ctypes
+    h = k3.k3moe_pool_header(magic=k3.K3MOE_POOL_MAGIC, version=k3.K3MOE_POOL_VERSION, d=7168, f=1536, E=896,
+                             s_min=121, s_max=125, zero_scales=0, expert_bytes=17547264)
+    for k_, v in kw.items():
+        setattr(h, k_, v)
+    raw = bytes(h)[:k3.k3moe_pool_header.checksum.offset]
+    h.checksum = _fnv1a64(raw)
+    return h
+
+
+def test_pool_header_check_accepts_a_valid_header_and_names_each_mismatch():
+    dm = k3.dims(7168, 1536, 896, 16, 1)
+    k3.k3moe_pool_header_check(_header(), dm)
+    cases = [(dict(magic=0x12345678), "magic"), (dict(version=2), "version"), (dict(E=895), "E=895"),
+             (dict(expert_bytes=17547263), "expert size"), (dict(s_min=126), "scale range"),
+             (dict(s_min=0, zero_scales=0), "scale range"), (dict(s_max=255), "scale range")]
+    for kw, needle in cases:
+        with pytest.raises(k3.K3MoEError) as ei:
+            k3.k3moe_pool_header_check(_header(**kw), dm)
+        assert ei.value.code == k3.K3MOE_ERR_INVALID_ARG and needle in str(ei.value), (kw, str(ei.value))
+    h = _header()
+    h.s_max = 124  # changed after the checksum was taken
+    with pytest.raises(k3.K3MoEError) as ei:
+        k3.k3moe_pool_header_check(h, dm)
+    assert "checksum" in str(ei.value)
+    with pytest.raises(k3.K3MoEError):
+        k3.k3moe_pool_header_check(_header(), k3.dims(7168, 1536, 896, 16, 0))  # invalid dims

@@ -368,3 +368,38 @@ def test_situ_glu_option_matches_oracle(path, T):
     with pytest.raises(k3.K3MoEError):
         k3.k3moe_set_option(L.layer, k3.K3MOE_OPT_ACTIVATION, 7)
     L.free()
+
+
+@pytest.mark.parametrize("src_on_device,cached", [(0, False), (1, False), (0, True)])
+def test_layer_from_saved_packed_pool_is_byte_identical(src_on_device, cached):
+    # a packed pool saved with its header (k3moe_read_packed per expert + k3moe_pool_header_get)
+    # loads into a new layer without repacking and gives the original layer's bytes
+    d, f, E, k, T = 512, 256, 16, 4, 6
+    L = Small(d, f, E, k, T, seed=91)
+    dm = k3.dims(d, f, E, k, T)
+    eb = k3.k3moe_packed_expert_bytes(dm)
+    hdr = k3.k3moe_pool_header_get(L.layer)
+    k3.k3moe_pool_header_check(hdr, dm)
+    assert (hdr.s_min, hdr.s_max, hdr.expert_bytes) == (int(L.scl.min()), int(L.scl.max()), eb)
+    pool = np.empty(E * eb, np.uint8)
+    for e in range(E):
+        k3.k3moe_read_packed(L.layer, e, pool[e * eb:(e + 1) * eb])
+    src = torch.from_numpy(pool).cuda() if src_on_device else pool
+    Wr = _dev(L.Wr) if src_on_device else L.Wr
+    cache = k3.k3moe_cache_create(8 * eb, eb) if cached else None
+    L2 = k3.k3moe_layer_from_packed(dm, hdr, src, src_on_device, Wr, None, cache)
+    try:
+        x = L.tokens(T)
+        y = torch.empty((T, d), dtype=torch.float32, device="cuda")
+        k3.k3moe_layer_forward(L2, _dev(x), T, y)
+        torch.cuda.synchronize()
+        assert np.array_equal(y.cpu().numpy(), L.forward(x))
+        bad = k3.k3moe_pool_header_get(L.layer)
+        bad.E = 15
+        with pytest.raises(k3.K3MoEError):
+            k3.k3moe_layer_from_packed(dm, bad, src, src_on_device, Wr)
+    finally:
+        k3.k3moe_layer_free(L2)
+        if cache is not None:
+            k3.k3moe_cache_destroy(cache)
+        L.free()
