@@ -424,6 +424,8 @@ def run_stack4(args):
     n_layers = 4
     budget = int(args.budget_gb * 1e9)
     cache = k3.k3moe_cache_create(budget, EXPERT_BYTES)
+    if args.device_lru:
+        k3.k3moe_cache_set_device_lru(cache, 1)
     nb, sb = synth.expert_bytes(D, F)
     layers = []
     for l in range(n_layers):
@@ -529,7 +531,7 @@ def run_stack4(args):
             "data": "synthetic (seeded splitmix64 experts, N(0,1) bf16 tokens, N(0,1/d) router)",
             "impl": "b300",
             "config": {"workload": WORKLOADS["stack4"]["desc"], "budget_gb": args.budget_gb,
-                       "miss_path": args.miss_path,
+                       "miss_path": "device-side LRU + zero-copy" if args.device_lru else args.miss_path,
                        "cache_slots": budget // EXPERT_BYTES, "tokens_per_step": n_tok, "layers": n_layers,
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                        "l2": "inputs larger than L2: 62.9 GB pool"},
@@ -694,6 +696,8 @@ def main():
     ap.add_argument("--budget-gb", type=float, default=8.0, help="stack4: device cache budget (1 GB = 1e9 B)")
     ap.add_argument("--miss-path", default="copy-engine", choices=["copy-engine", "zero-copy"],
                     help="stack4: how missed experts reach their slots (K3MOE_OPT_MISS_PATH)")
+    ap.add_argument("--device-lru", action="store_true",
+                    help="stack4: the cache keeps its LRU state on the device (k3moe_cache_set_device_lru)")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--experts", type=int, default=E,

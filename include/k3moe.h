@@ -286,6 +286,18 @@ void k3moe_layer_free(k3moe_layer* layer);
  * Least-recently-used experts are replaced; misses are copied from the layer's pinned pool
  * on a side stream.  Errors: INVALID_ARG (budget < one slot), OOM, CUDA. */
 int k3moe_cache_create(size_t budget_bytes, size_t slot_bytes, k3moe_cache** out);
+/* Keep the cache's LRU state on the device instead of the host (enable = 1; allowed only while no
+ * layer uses the cache).  A layer call then looks its experts up with a one-thread kernel on its
+ * own stream right after routing and copies the misses into their slots with the zero-copy kernel
+ * (the SMs read the layer's mapped pinned pool): no host round trip between routing and the FFN,
+ * so cache-mode calls queue like device-resident ones.  The policy and the statistics are those of
+ * the host bookkeeping (hits made most recently used first, then each miss takes the least
+ * recently used slot).  Because the device lookup cannot refuse a call, a layer attaches only when
+ * min(E, T_max * k) <= slots (else K3MOE_ERR_BUDGET_TOO_SMALL from k3moe_pack_experts,
+ * k3moe_layer_from_packed or k3moe_layer_set_cache).  Calls of layers sharing one cache must be
+ * ordered (one stream).  K3MOE_OPT_MISS_PATH does not apply.  Errors: INVALID_ARG (NULL, layers
+ * attached), OOM, CUDA. */
+int k3moe_cache_set_device_lru(k3moe_cache* cache, int enable);
 /* Waits for the layer calls it counts (a device synchronisation when some calls skipped the
  * lookup: their expert counts are read back asynchronously). */
 int k3moe_cache_stats(const k3moe_cache* cache, k3moe_cache_stats_t* out);

@@ -89,6 +89,7 @@ _SIGS = {
     "k3moe_cache_simulate": ([_vp, _vp, _i, _i, _i, ctypes.c_ulonglong, ctypes.POINTER(k3moe_cache_sim_stats)], _i),
     "k3moe_last_error": ([], ctypes.c_char_p),
     "k3moe_router_topk_noalloc": ([_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp], _i),
+    "k3moe_cache_set_device_lru": ([_vp, _i], _i),
     "k3moe_pool_header_get": ([_vp, ctypes.POINTER(k3moe_pool_header)], _i),
     "k3moe_pool_header_check": ([ctypes.POINTER(k3moe_pool_header), ctypes.POINTER(k3moe_dims)], _i),
     "k3moe_layer_from_packed": ([ctypes.POINTER(k3moe_dims), ctypes.POINTER(k3moe_pool_header), _vp, _i, _vp, _vp,
@@ -246,6 +247,10 @@ def k3moe_cache_stats(cache) -> dict:
     st = k3moe_cache_stats_t()
     _check(_lib.k3moe_cache_stats(_handle(cache), ctypes.byref(st)))
     return {n: getattr(st, n) for n, _ in st._fields_}
+
+
+def k3moe_cache_set_device_lru(cache, enable: int) -> None:
+    _check(_lib.k3moe_cache_set_device_lru(_handle(cache), int(enable)))
 
 
 def k3moe_cache_reset_stats(cache) -> None:

@@ -86,6 +86,12 @@ struct k3moe_cache {
   static constexpr int kRing = 4096;
   int32_t* ring = nullptr;
   int ring_n = 0;
+  // device-side LRU (k3moe_cache_set_device_lru): the state the lookup kernel keeps
+  bool device_lru = false;
+  LruState* d_state = nullptr;
+  int32_t* d_prev = nullptr;
+  int32_t* d_next = nullptr;
+  int32_t** d_owner = nullptr;
 };
 
 struct k3moe_layer {
@@ -97,6 +103,8 @@ struct k3moe_layer {
   MissCopy* miss_host = nullptr;  // pinned [E]: a call's misses (zero-copy miss path)
   MissCopy* miss_dev = nullptr;   // device [E]
   int miss_path = K3MOE_MISS_COPY_ENGINE;
+  int32_t* d_slot_of = nullptr;   // device [E]: expert -> slot (device-side LRU)
+  int32_t* d_nmiss = nullptr;     // device [1]: the last call's misses (device-side LRU)
   float* Wr = nullptr;          // device [E][d]
   uint16_t* Wsplit = nullptr;   // device [E][2d] bf16: W_r rounded (hi) then the rounding remainder (lo)
   float* bias = nullptr;        // device [E] or nullptr
@@ -205,18 +213,36 @@ cudaError_t fold_ring(k3moe_cache* C) {
   return cudaSuccess;
 }
 
-void attach_cache(k3moe_layer* L, k3moe_cache* C) {
+int attach_cache(k3moe_layer* L, k3moe_cache* C) {
+  if (C->device_lru) {
+    // the lookup kernel cannot refuse a call: every call must fit in the slots
+    const long long need = std::min<long long>(L->dims.E, (long long)L->dims.T_max * L->dims.k);
+    if (need > C->n_slots)
+      return fail(K3MOE_ERR_BUDGET_TOO_SMALL, "a call may need %lld experts resident, the cache has %d slots", need,
+                  C->n_slots);
+    if (!L->d_slot_of && (cudaMalloc((void**)&L->d_slot_of, (size_t)L->dims.E * 4) != cudaSuccess ||
+                          cudaMalloc((void**)&L->d_nmiss, 4) != cudaSuccess)) {
+      cudaGetLastError();
+      return fail(K3MOE_ERR_OOM, "device-side cache tables could not be allocated");
+    }
+    CUDA_TRY(cudaMemset(L->d_slot_of, 0xFF, (size_t)L->dims.E * 4));  // -1: not resident
+  }
   L->cache = C;
   L->uid = C->next_uid++;
   C->users += 1;
   C->experts_attached += L->dims.E;
   C->resident[L->uid] = 0;
+  return K3MOE_OK;
 }
 
 // Drops the layer's experts from its cache: their slots become free (least recently used).
 void detach_cache(k3moe_layer* L) {
   k3moe_cache* C = L->cache;
   if (!C) return;
+  if (C->device_lru && L->d_slot_of) {
+    launch_lru_detach(C->d_state, C->d_prev, C->d_next, C->d_owner, C->n_slots, L->d_slot_of, L->dims.E, nullptr);
+    cudaDeviceSynchronize();
+  }
   fold_ring(C);
   C->experts_attached -= L->dims.E;
   C->resident.erase(L->uid);
@@ -257,6 +283,8 @@ void free_layer(k3moe_layer* L) {
   for (auto e : L->spare_events) cudaEventDestroy(e);
   if (L->copies_done) cudaEventDestroy(L->copies_done);
   detach_cache(L);
+  cudaFree(L->d_slot_of);
+  cudaFree(L->d_nmiss);
   delete L;
 }
 
@@ -314,6 +342,22 @@ int run_routing(k3moe_layer* L, const void* x, int T, cudaStream_t s, bool need_
 int make_resident(k3moe_layer* L, cudaStream_t s) {
   k3moe_cache* C = L->cache;
   const int E = L->dims.E;
+  if (C->device_lru) {
+    // lookup and copies on the device, on `s`: no host round trip
+    LruArgs la{C->d_state, C->d_prev, C->d_next, C->d_owner, C->n_slots, C->slots, C->slot_bytes, L->ws.act,
+               L->ws.nact, L->d_slot_of, (const uint8_t**)L->eptr_dev, L->pool_dev, L->miss_dev, L->d_nmiss,
+               L->ws.sync + 1};
+    cudaEvent_t a, b;
+    if (!C->free_events.empty()) { a = C->free_events.back(); C->free_events.pop_back(); } else cudaEventCreate(&a);
+    if (!C->free_events.empty()) { b = C->free_events.back(); C->free_events.pop_back(); } else cudaEventCreate(&b);
+    CUDA_TRY(launch_lru_lookup(la, s));
+    CUDA_TRY(cudaEventRecord(a, s));
+    CUDA_TRY(launch_miss_copy_dev(L->miss_dev, L->d_nmiss, std::min(E, L->dims.T_max * L->dims.k), L->exp_bytes,
+                                  L->num_sms, s));
+    CUDA_TRY(cudaEventRecord(b, s));
+    C->pending.emplace_back(a, b);
+    return K3MOE_OK;
+  }
   if ((long long)C->n_slots >= C->experts_attached && C->resident[L->uid] == E) {
     // every expert of the layer has a slot and nothing can be evicted: the pointer table on
     // the device is complete, so no lookup (and no host round trip) is needed
@@ -574,6 +618,16 @@ int k3moe_cache_stats(const k3moe_cache* cc, k3moe_cache_stats_t* out) {
   if (!cc || !out) return fail(K3MOE_ERR_INVALID_ARG, "NULL argument");
   k3moe_cache* C = const_cast<k3moe_cache*>(cc);
   CUDA_TRY(fold_ring(C));
+  if (C->device_lru) {
+    LruState st;
+    CUDA_TRY(cudaDeviceSynchronize());
+    CUDA_TRY(cudaMemcpy(&st, C->d_state, sizeof(st), cudaMemcpyDeviceToHost));
+    C->st.hits = st.hits;
+    C->st.misses = st.misses;
+    C->st.evictions = st.evictions;
+    C->st.calls = st.calls;
+    C->st.h2d_bytes = st.misses * C->slot_bytes;
+  }
   for (auto& pr : C->pending) {
     float ms = 0.f;
     if (cudaEventSynchronize(pr.second) == cudaSuccess && cudaEventElapsedTime(&ms, pr.first, pr.second) == cudaSuccess)
@@ -591,6 +645,12 @@ int k3moe_cache_reset_stats(k3moe_cache* C) {
   k3moe_cache_stats_t tmp;
   k3moe_cache_stats(C, &tmp);
   C->st = k3moe_cache_stats_t{};
+  if (C->device_lru) {
+    LruState st;
+    CUDA_TRY(cudaMemcpy(&st, C->d_state, sizeof(st), cudaMemcpyDeviceToHost));
+    st.hits = st.misses = st.evictions = st.calls = 0;
+    CUDA_TRY(cudaMemcpy(C->d_state, &st, sizeof(st), cudaMemcpyHostToDevice));
+  }
   return K3MOE_OK;
 }
 
@@ -607,7 +667,55 @@ void k3moe_cache_destroy(k3moe_cache* C) {
   for (auto e : C->free_events) cudaEventDestroy(e);
   cudaFree(C->slots);
   cudaFreeHost(C->ring);
+  cudaFree(C->d_state);
+  cudaFree(C->d_prev);
+  cudaFree(C->d_next);
+  cudaFree((void*)C->d_owner);
   delete C;
+}
+
+int k3moe_cache_set_device_lru(k3moe_cache* C, int enable) {
+  if (!C) return fail(K3MOE_ERR_INVALID_ARG, "cache is NULL");
+  if (enable != 0 && enable != 1) return fail(K3MOE_ERR_INVALID_ARG, "enable must be 0 or 1");
+  if (C->users != 0) return fail(K3MOE_ERR_INVALID_ARG, "the cache already serves %d layers", C->users);
+  if ((enable != 0) == C->device_lru) return K3MOE_OK;
+  if (!enable) {
+    cudaFree(C->d_state);
+    cudaFree(C->d_prev);
+    cudaFree(C->d_next);
+    cudaFree((void*)C->d_owner);
+    C->d_state = nullptr;
+    C->d_prev = C->d_next = nullptr;
+    C->d_owner = nullptr;
+    C->device_lru = false;
+    return K3MOE_OK;
+  }
+  const int n = C->n_slots;
+  if (cudaMalloc((void**)&C->d_state, sizeof(LruState)) != cudaSuccess ||
+      cudaMalloc((void**)&C->d_prev, (size_t)n * 4) != cudaSuccess ||
+      cudaMalloc((void**)&C->d_next, (size_t)n * 4) != cudaSuccess ||
+      cudaMalloc((void**)&C->d_owner, (size_t)n * sizeof(int32_t*)) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(C->d_state);
+    cudaFree(C->d_prev);
+    cudaFree(C->d_next);
+    C->d_state = nullptr;
+    C->d_prev = C->d_next = nullptr;
+    return fail(K3MOE_ERR_OOM, "device-side cache state could not be allocated");
+  }
+  // the host bookkeeping's initial order: slot 0 most recently used ... slot n-1 least
+  std::vector<int32_t> prev(n), next(n);
+  for (int i = 0; i < n; ++i) {
+    prev[i] = i - 1;
+    next[i] = i + 1 < n ? i + 1 : -1;
+  }
+  LruState st{0, n - 1, 0, 0, 0, 0};
+  CUDA_TRY(cudaMemcpy(C->d_prev, prev.data(), (size_t)n * 4, cudaMemcpyHostToDevice));
+  CUDA_TRY(cudaMemcpy(C->d_next, next.data(), (size_t)n * 4, cudaMemcpyHostToDevice));
+  CUDA_TRY(cudaMemset((void*)C->d_owner, 0, (size_t)n * sizeof(int32_t*)));
+  CUDA_TRY(cudaMemcpy(C->d_state, &st, sizeof(st), cudaMemcpyHostToDevice));
+  C->device_lru = true;
+  return K3MOE_OK;
 }
 
 }  // extern "C"
@@ -695,7 +803,8 @@ int layer_finish(k3moe_layer* L, cudaStream_t s) {
   } else {
     k3moe_cache* C = L->cache;
     L->cache = nullptr;
-    attach_cache(L, C);
+    const int rc = attach_cache(L, C);
+    if (rc) return rc;
   }
   L->last_stream = s;
   return K3MOE_OK;
@@ -884,9 +993,14 @@ int k3moe_layer_set_cache(k3moe_layer* L, k3moe_cache* C) {
   if (C == L->cache) return K3MOE_OK;
   if (L->last_stream) CUDA_TRY(cudaStreamSynchronize(L->last_stream));
   if (L->cache) CUDA_TRY(cudaStreamSynchronize(L->cache->copy_stream));
+  if (C->device_lru) {
+    const long long need = std::min<long long>(L->dims.E, (long long)L->dims.T_max * L->dims.k);
+    if (need > C->n_slots)
+      return fail(K3MOE_ERR_BUDGET_TOO_SMALL, "a call may need %lld experts resident, the cache has %d slots", need,
+                  C->n_slots);
+  }
   detach_cache(L);
-  attach_cache(L, C);
-  return K3MOE_OK;
+  return attach_cache(L, C);
 }
 
 int k3moe_router_topk(k3moe_layer* L, const void* x, int T, int32_t* idx, float* w, void* stream) {

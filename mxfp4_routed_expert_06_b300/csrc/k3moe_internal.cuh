@@ -188,6 +188,7 @@ __device__ __forceinline__ float gate_act(float g, int act) {
 // Device error flags (ws.sync[1]).
 constexpr uint32_t kErrTimeout = 1u;
 constexpr uint32_t kErrBadAccess = 2u;  // self-checking builds only: a copy address failed its check
+constexpr uint32_t kErrBudget = 4u;     // device-side cache lookup: a call needed more experts than slots
 
 struct FfnArgs {
   const uint8_t* const* expert_ptr;  // [E] device pointers to each expert's packed block
@@ -250,6 +251,34 @@ struct MissCopy {
   uint8_t* dst;        // its device slot
 };
 cudaError_t launch_miss_copy(const MissCopy* list, int n, size_t bytes, int num_sms, cudaStream_t s);
+
+// Device-side LRU of the expert cache (k3moe_cache_set_device_lru).
+struct LruState {
+  int head, tail;                                  // most / least recently used slot (-1: none)
+  unsigned long long hits, misses, evictions, calls;
+};
+struct LruArgs {
+  LruState* state;
+  int32_t* prev;            // [n_slots] LRU list links
+  int32_t* next;
+  int32_t** owner;          // [n_slots] the layer's slot_of entry that holds the slot, or null
+  int n_slots;
+  uint8_t* slots;           // slot s at slots + s * slot_bytes
+  size_t slot_bytes;
+  const int32_t* act;       // [nact] active experts of the call, ascending
+  const int32_t* nact;
+  int32_t* slot_of;         // [E] the layer's expert -> slot (-1: not resident)
+  const uint8_t** eptr;     // [E] device pointer table the FFN kernels read
+  const uint8_t* pool_dev;  // the layer's mapped pinned pool
+  MissCopy* miss;           // [E] out: the call's misses
+  int32_t* nmiss;           // out: their count
+  uint32_t* err;            // device error flags
+};
+cudaError_t launch_lru_lookup(const LruArgs& a, cudaStream_t s);
+cudaError_t launch_miss_copy_dev(const MissCopy* list, const int32_t* n_dev, int max_n, size_t bytes, int num_sms,
+                                 cudaStream_t s);
+cudaError_t launch_lru_detach(LruState* st, int32_t* prev, int32_t* next, int32_t** owner, int n_slots,
+                              const int32_t* slot_of, int E, cudaStream_t s);
 
 // canon_nib/canon_scl point at the canonical bytes of the first of n_exp experts; dst at its packed block.
 cudaError_t launch_pack(const uint8_t* canon_nib, const uint8_t* canon_scl, int n_exp, int d, int f, uint8_t* dst,

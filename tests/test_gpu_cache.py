@@ -224,6 +224,58 @@ def test_zero_copy_miss_path_matches_copy_engine():
         k3.k3moe_layer_free(L)
 
 
+def test_device_side_lru_matches_host_bookkeeping():
+    """The cache with its LRU state on the device (lookup kernel + zero-copy miss copies, no host
+    round trip): the same bytes as the device-resident layers and the same hits, misses and
+    evictions as the host bookkeeping, also across a move to another device-side cache; layers
+    that might need more experts than the cache has slots are refused when they attach."""
+    d, f, E, k, T, n_layers, steps = 512, 256, 32, 4, 3, 2, 16
+    dm = k3.dims(d, f, E, k, T)
+    eb = k3.k3moe_packed_expert_bytes(dm)
+    host = [synth.experts(17, l, 0, E, d, f) for l in range(n_layers)]
+    Wr = [synth.router_weights(17, l, E, d) for l in range(n_layers)]
+    x0 = [torch.from_numpy(synth.tokens_bf16(17, 0, s * T, T, d).view(np.int16)).cuda() for s in range(steps)]
+    dev = [k3.k3moe_pack_experts(dm, host[l][0], host[l][1], 0, Wr[l]) for l in range(n_layers)]
+    y_ref, _ = _run_stack(dev, x0, T, steps, d)
+    stats = {}
+    for device_lru in (0, 1):
+        cache = k3.k3moe_cache_create(E * eb, eb)
+        k3.k3moe_cache_set_device_lru(cache, device_lru)
+        layers = [k3.k3moe_pack_experts(dm, host[l][0], host[l][1], 0, Wr[l], None, cache) for l in range(n_layers)]
+        if device_lru:
+            with pytest.raises(k3.K3MoEError) as ei:  # layers attached: the mode is fixed
+                k3.k3moe_cache_set_device_lru(cache, 0)
+            assert ei.value.code == k3.K3MOE_ERR_INVALID_ARG
+        y, _ = _run_stack(layers, x0, T, steps, d)
+        assert np.array_equal(y, y_ref), f"device_lru={device_lru}: y differs from the device-resident layers"
+        st = k3.k3moe_cache_stats(cache)
+        assert st["misses"] > 0 and st["evictions"] > 0 and st["h2d_bytes"] == st["misses"] * eb
+        stats[device_lru] = (st["hits"], st["misses"], st["evictions"], st["calls"])
+        if device_lru:
+            other = k3.k3moe_cache_create(E * eb, eb)
+            k3.k3moe_cache_set_device_lru(other, 1)
+            for L in layers:
+                k3.k3moe_layer_set_cache(L, other)
+            y2, _ = _run_stack(layers, x0, T, steps, d)
+            assert np.array_equal(y2, y_ref)
+            st2 = k3.k3moe_cache_stats(other)
+            assert st2["misses"] > 0 and st2["calls"] == steps * n_layers
+        for L in layers:
+            k3.k3moe_layer_free(L)
+        k3.k3moe_cache_destroy(cache)
+        if device_lru:
+            k3.k3moe_cache_destroy(other)
+    assert stats[0] == stats[1]
+    tiny = k3.k3moe_cache_create(10 * eb, eb)  # T_max * k = 12 experts may be needed at once
+    k3.k3moe_cache_set_device_lru(tiny, 1)
+    with pytest.raises(k3.K3MoEError) as ei:
+        k3.k3moe_pack_experts(dm, host[0][0], host[0][1], 0, Wr[0], None, tiny)
+    assert ei.value.code == k3.K3MOE_ERR_BUDGET_TOO_SMALL
+    k3.k3moe_cache_destroy(tiny)
+    for L in dev:
+        k3.k3moe_layer_free(L)
+
+
 def test_budget_too_small_then_recovers():
     d, f, E, k, T = 256, 128, 16, 4, 2
     dm = k3.dims(d, f, E, k, T)

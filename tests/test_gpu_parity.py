@@ -386,7 +386,7 @@ def test_layer_from_saved_packed_pool_is_byte_identical(src_on_device, cached):
         k3.k3moe_read_packed(L.layer, e, pool[e * eb:(e + 1) * eb])
     src = torch.from_numpy(pool).cuda() if src_on_device else pool
     Wr = _dev(L.Wr) if src_on_device else L.Wr
-    cache = k3.k3moe_cache_create(8 * eb, eb) if cached else None
+    cache = k3.k3moe_cache_create(E * eb, eb) if cached else None
     L2 = k3.k3moe_layer_from_packed(dm, hdr, src, src_on_device, Wr, None, cache)
     try:
         x = L.tokens(T)
