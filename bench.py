@@ -447,17 +447,60 @@ def run_stack4(args):
 
     resid = torch.empty((1, D), dtype=torch.int16, device="cuda")
     xin = torch.empty((1, D), dtype=torch.int16, device="cuda")
+    idx = torch.empty((1, K), dtype=torch.int32, device="cuda")
+    wts = torch.empty((1, K), dtype=torch.float32, device="cuda")
 
-    def step():
-        # layer 0 takes the token; then r = bf16(r + y) and the next layer takes RMSNorm(r)
+    def record_trace():
+        # the expert set each call of a step looks up, from the library's own top-k on the same
+        # layer inputs (one untimed step)
+        trace = []
         for t in range(n_tok):
             x = xd[t:t + 1]
             resid.copy_(x)
             for l, L in enumerate(layers):
+                k3.k3moe_router_topk(L, x, 1, idx, wts, stream)
+                trace.append([l * E + int(e) for e in np.unique(idx.cpu().numpy())])
                 y = ys[t, l:l + 1]
                 k3.k3moe_layer_forward(L, x, 1, y, stream)
                 k3.k3moe_residual_rmsnorm(y, resid, 1, D, 1e-6, resid, xin, stream)
                 x = xin
+        torch.cuda.synchronize()
+        return trace
+
+    # Prefetch of the next call's experts while this call computes (k3moe_cache_prefetch):
+    # "trace" lists the set the next call will look up (recorded in an untimed step before the
+    # warm-up: the most any predictor can gain); "router" guesses it with the next layer's router
+    # on this layer's input (for the next token's first layer, on that token: exact).
+    trace = record_trace() if args.prefetch == "trace" else None
+    pidx = torch.empty((1, K), dtype=torch.int32, device="cuda")
+    pidx_host = torch.empty((1, K), dtype=torch.int32).pin_memory()
+    guess_ready = torch.cuda.Event()
+
+    def step():
+        # layer 0 takes the token; then r = bf16(r + y) and the next layer takes RMSNorm(r)
+        c = 0
+        for t in range(n_tok):
+            x = xd[t:t + 1]
+            resid.copy_(x)
+            for l, L in enumerate(layers):
+                nxt = layers[(l + 1) % n_layers]
+                if args.prefetch == "router":
+                    guess_in = x if l + 1 < n_layers else xd[(t + 1) % n_tok:(t + 1) % n_tok + 1]
+                    k3.k3moe_router_topk(nxt, guess_in, 1, pidx, wts, stream)
+                    pidx_host.copy_(pidx, non_blocking=True)
+                    guess_ready.record(stream)
+                y = ys[t, l:l + 1]
+                k3.k3moe_layer_forward(L, x, 1, y, stream)
+                # the FFN of this call is still running while the next call's experts come in
+                if args.prefetch == "router":
+                    guess_ready.synchronize()  # the router and the copy only (the FFN is queued after)
+                    k3.k3moe_cache_prefetch(nxt, np.unique(pidx_host.numpy()))
+                elif args.prefetch == "trace":
+                    nc = (c + 1) % len(trace)
+                    k3.k3moe_cache_prefetch(nxt, [e - ((nc % n_layers) * E) for e in trace[nc]])
+                k3.k3moe_residual_rmsnorm(y, resid, 1, D, 1e-6, resid, xin, stream)
+                x = xin
+                c += 1
 
     for _ in range(args.warmup):
         step()
@@ -497,27 +540,17 @@ def run_stack4(args):
     # timed steps through the same number of slots under LRU (the device cache's policy),
     # Belady's MIN and random replacement; hit rates over the timed steps.
     slots = budget // EXPERT_BYTES
-    trace = []
-    idx = torch.empty((1, K), dtype=torch.int32, device="cuda")
-    wts = torch.empty((1, K), dtype=torch.float32, device="cuda")
-    for t in range(n_tok):
-        x = xd[t:t + 1]
-        resid.copy_(x)
-        for l, L in enumerate(layers):
-            k3.k3moe_router_topk(L, x, 1, idx, wts, stream)
-            trace.append([l * E + int(e) for e in np.unique(idx.cpu().numpy())])
-            y = ys[t, l:l + 1]
-            k3.k3moe_layer_forward(L, x, 1, y, stream)
-            k3.k3moe_residual_rmsnorm(y, resid, 1, D, 1e-6, resid, xin, stream)
-            x = xin
-    torch.cuda.synchronize()
+    if trace is None:
+        trace = record_trace()
     study = {}
     for name, pol in (("lru", k3.K3MOE_POLICY_LRU), ("min", k3.K3MOE_POLICY_MIN), ("random", k3.K3MOE_POLICY_RANDOM)):
         warm = k3.k3moe_cache_simulate(trace * args.warmup, slots, pol, SEED)
         full = k3.k3moe_cache_simulate(trace * (args.warmup + args.steps), slots, pol, SEED)
         h, m = full["hits"] - warm["hits"], full["misses"] - warm["misses"]
         study[name] = {"hits": h, "misses": m, "hit_rate": round(h / max(1, h + m), 4)}
-    study["lru_equals_device"] = (study["lru"]["hits"], study["lru"]["misses"]) == (st["hits"], st["misses"])
+    # without prefetch the device cache must count what the simulated LRU counts
+    study["lru_equals_device"] = ((study["lru"]["hits"], study["lru"]["misses"]) == (st["hits"], st["misses"])
+                                  if args.prefetch == "none" else None)
     value, ms = job_throughput(n_tok * args.steps, ms, pg)
     hbm_peak, _, peak_kind = _peaks()
     gu_ms, gu_n = prof.get("gateup", (0.0, 0))
@@ -532,10 +565,12 @@ def run_stack4(args):
             "impl": "b300",
             "config": {"workload": WORKLOADS["stack4"]["desc"], "budget_gb": args.budget_gb,
                        "miss_path": "device-side LRU + zero-copy" if args.device_lru else args.miss_path,
+                       "prefetch": args.prefetch,
                        "cache_slots": budget // EXPERT_BYTES, "tokens_per_step": n_tok, "layers": n_layers,
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                        "l2": "inputs larger than L2: 62.9 GB pool"},
             "cache": {"hits": st["hits"], "misses": st["misses"], "evictions": st["evictions"],
+                      "prefetched": st["prefetched"],
                       "hit_rate": round(st["hits"] / max(1, st["hits"] + st["misses"]), 4),
                       "h2d_gb": round(st["h2d_bytes"] / 1e9, 3),
                       "h2d_gbs_of_copy_time": round(st["h2d_bytes"] / 1e6 / max(st["h2d_ms"], 1e-9), 2),
@@ -698,6 +733,10 @@ def main():
                     help="stack4: how missed experts reach their slots (K3MOE_OPT_MISS_PATH)")
     ap.add_argument("--device-lru", action="store_true",
                     help="stack4: the cache keeps its LRU state on the device (k3moe_cache_set_device_lru)")
+    ap.add_argument("--prefetch", choices=["none", "trace", "router"], default="none",
+                    help="stack4: while a call computes, prefetch the next call's experts (k3moe_cache_prefetch): "
+                         "'trace' = the set it will look up (recorded before the warm-up), 'router' = the next "
+                         "layer's router on this layer's input")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--experts", type=int, default=E,
@@ -706,6 +745,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.prefetch != "none" and args.device_lru:
+        ap.error("--prefetch needs the host-side LRU bookkeeping (not --device-lru)")
     if args.tokens_per_step is None:
         args.tokens_per_step = 256 if args.workload == "stack4" else 1000
     if args.impl == "reference":

@@ -74,6 +74,8 @@ typedef struct {
   uint64_t h2d_bytes;  /* bytes copied host -> device by misses */
   double h2d_ms;       /* device time of those copies (CUDA events on the copy stream) */
   uint64_t calls;      /* layer calls served */
+  uint64_t prefetched; /* experts copied by k3moe_cache_prefetch (their bytes are in h2d_bytes and
+                          their copy time in h2d_ms; a later call that finds one counts a hit) */
 } k3moe_cache_stats_t;
 
 /* Bytes of one expert in the packed device layout (equal to the canonical byte count:
@@ -304,6 +306,24 @@ int k3moe_cache_stats(const k3moe_cache* cache, k3moe_cache_stats_t* out);
 int k3moe_cache_reset_stats(k3moe_cache* cache);
 /* Destroy after every layer that uses it has been freed or moved to another cache. */
 void k3moe_cache_destroy(k3moe_cache* cache);
+/* Prefetch ("four reductions", expert LRU paragraph: the engine's cache loads the experts a
+ * batch needs ahead of the arithmetic).  Makes experts[0..n) of `layer` resident in its cache
+ * before a later call asks for them, so that the copies overlap work already queued:
+ *   experts  host int32 [n], ids in 0..E-1 (duplicates allowed); n >= 0
+ *   fetched  host int (may be NULL): the number of experts this call copied
+ * Listed experts already resident become most recently used.  Each other listed expert, in list
+ * order, takes the least recently used slot and is copied from the layer's pinned pool on the
+ * cache's copy stream; this call does not wait for the copies.  A slot that a layer call still in
+ * flight may read is never taken, nor one holding an expert the list names: the prefetch stops
+ * at the first such slot, and `fetched` tells how far it got.  A call is known to have finished once a later call of a layer on this cache
+ * has looked up its experts (that lookup waits for the stream) or after k3moe_sync.  The next
+ * layer call that uses a prefetched expert waits on its stream for the prefetch copies; its
+ * output is unchanged (only which copies run, and when, differs).  Relies on the layers that
+ * share a cache making their calls on one stream.  Errors: INVALID_ARG (NULL layer, a layer
+ * without a cache, n < 0, experts NULL with n > 0, an id out of range: nothing is done),
+ * UNSUPPORTED (the cache keeps its LRU state on the device), CUDA (a copy could not be issued:
+ * its slot is forgotten, the copies issued before it stay valid). */
+int k3moe_cache_prefetch(k3moe_layer* layer, const int32_t* experts, int n, int* fetched);
 /* Moves a layer packed in cache mode (its experts in a pinned host pool) to another cache
  * with the same slot_bytes, e.g. to run the same layers under a different memory budget.
  * Waits for the layer's last stream, then drops the layer's experts from its old cache (its

@@ -48,7 +48,8 @@ class k3moe_dims(ctypes.Structure):
 
 class k3moe_cache_stats_t(ctypes.Structure):
     _fields_ = [("hits", ctypes.c_uint64), ("misses", ctypes.c_uint64), ("evictions", ctypes.c_uint64),
-                ("h2d_bytes", ctypes.c_uint64), ("h2d_ms", ctypes.c_double), ("calls", ctypes.c_uint64)]
+                ("h2d_bytes", ctypes.c_uint64), ("h2d_ms", ctypes.c_double), ("calls", ctypes.c_uint64),
+                ("prefetched", ctypes.c_uint64)]
 
 
 class k3moe_cache_sim_stats(ctypes.Structure):
@@ -90,6 +91,7 @@ _SIGS = {
     "k3moe_last_error": ([], ctypes.c_char_p),
     "k3moe_router_topk_noalloc": ([_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp], _i),
     "k3moe_cache_set_device_lru": ([_vp, _i], _i),
+    "k3moe_cache_prefetch": ([_vp, _vp, _i, ctypes.POINTER(_i)], _i),
     "k3moe_pool_header_get": ([_vp, ctypes.POINTER(k3moe_pool_header)], _i),
     "k3moe_pool_header_check": ([ctypes.POINTER(k3moe_pool_header), ctypes.POINTER(k3moe_dims)], _i),
     "k3moe_layer_from_packed": ([ctypes.POINTER(k3moe_dims), ctypes.POINTER(k3moe_pool_header), _vp, _i, _vp, _vp,
@@ -251,6 +253,17 @@ def k3moe_cache_stats(cache) -> dict:
 
 def k3moe_cache_set_device_lru(cache, enable: int) -> None:
     _check(_lib.k3moe_cache_set_device_lru(_handle(cache), int(enable)))
+
+
+def k3moe_cache_prefetch(layer, experts) -> int:
+    """Makes the listed experts of a cache-mode layer resident ahead of use; returns how many were
+    copied (fewer than the missing ones when the remaining slots belong to calls still in flight)."""
+    import numpy as np
+    ids = np.ascontiguousarray(np.asarray(experts, dtype=np.int32).reshape(-1))
+    got = _i(0)
+    _check(_lib.k3moe_cache_prefetch(_handle(layer), ids.ctypes.data if ids.size else None, int(ids.size),
+                                     ctypes.byref(got)))
+    return got.value
 
 
 def k3moe_cache_reset_stats(cache) -> None:

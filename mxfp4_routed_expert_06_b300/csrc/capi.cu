@@ -1,5 +1,6 @@
 // capi.cu -- the C ABI (include/k3moe.h): argument checks, ownership, workspace, dispatch,
 // and the expert cache's host-side LRU bookkeeping.
+#include <algorithm>
 #include <cstdarg>
 #include <cstddef>
 #include <cstdio>
@@ -92,6 +93,16 @@ struct k3moe_cache {
   int32_t* d_prev = nullptr;
   int32_t* d_next = nullptr;
   int32_t** d_owner = nullptr;
+  // Ordering of prefetches (k3moe_cache_prefetch) against the calls still in flight.  Calls get
+  // increasing serials; a slot remembers the serial of the last call (or prefetch) that touched it.
+  // The host LRU list, read from its back, holds the empty slots and then the filled ones in
+  // nondecreasing serial, so the first slot a prefetch may not take ends its evictions.
+  std::vector<long long> slot_call;
+  long long calls_issued = 0;          // serial of the next call or prefetch
+  long long done_before = 0;           // every call with a smaller serial has finished on the device
+  bool fast_since_sync = false;        // a call skipped the lookup (touching no serial) since then
+  cudaEvent_t prefetch_done = nullptr; // recorded on the copy stream after the last prefetch's copies
+  bool prefetch_pending = false;
 };
 
 struct k3moe_layer {
@@ -365,11 +376,25 @@ int make_resident(k3moe_layer* L, cudaStream_t s) {
     CUDA_TRY(cudaMemcpyAsync(C->ring + C->ring_n, L->ws.nact, 4, cudaMemcpyDeviceToHost, s));
     C->ring_n += 1;
     C->st.calls += 1;
+    C->calls_issued += 1;
+    C->fast_since_sync = true;
+    if (C->prefetch_pending) CUDA_TRY(cudaStreamWaitEvent(s, C->prefetch_done, 0));  // a prefetched slot
     return K3MOE_OK;
   }
   CUDA_TRY(cudaMemcpyAsync(L->act_host, L->ws.nact, 4, cudaMemcpyDeviceToHost, s));
   CUDA_TRY(cudaMemcpyAsync(L->act_host + 1, L->ws.act, (size_t)E * 4, cudaMemcpyDeviceToHost, s));
   CUDA_TRY(cudaStreamSynchronize(s));
+  // every earlier call (one stream) has finished: their slots are free for a prefetch to take
+  const long long serial = C->calls_issued++;
+  C->done_before = serial;
+  C->fast_since_sync = false;
+  if (C->prefetch_pending) {
+    // this call's hits, and the slots its misses take, may still be receiving prefetch copies
+    if (cudaEventQuery(C->prefetch_done) == cudaSuccess)
+      C->prefetch_pending = false;
+    else
+      CUDA_TRY(cudaStreamWaitEvent(s, C->prefetch_done, 0));
+  }
   const int nact = L->act_host[0];
   if (nact < 0 || nact > E) return fail(K3MOE_ERR_CUDA, "corrupt active-expert count %d", nact);
   if (nact > C->n_slots)
@@ -385,6 +410,7 @@ int make_resident(k3moe_layer* L, cudaStream_t s) {
       C->lru.erase(C->lru_pos[slot]);
       C->lru.push_front(slot);
       C->lru_pos[slot] = C->lru.begin();
+      C->slot_call[slot] = serial;
       L->eptr_host[act[i]] = C->slots + (size_t)slot * C->slot_bytes;
       C->st.hits += 1;
     } else {
@@ -422,6 +448,7 @@ int make_resident(k3moe_layer* L, cudaStream_t s) {
       C->where[key] = slot;
       C->lru.push_front(slot);
       C->lru_pos[slot] = C->lru.begin();
+      C->slot_call[slot] = serial;
       uint8_t* dst = C->slots + (size_t)slot * C->slot_bytes;
       const bool fake = L->test_fail_copy > 0 && --L->test_fail_copy == 0;  // failure-path test
       cudaError_t ce = cudaSuccess;
@@ -606,6 +633,7 @@ int k3moe_cache_create(size_t budget_bytes, size_t slot_bytes, k3moe_cache** out
   }
   C->lru_pos.resize(n);
   C->slot_key.assign(n, -1);
+  C->slot_call.assign(n, -1);
   for (int i = 0; i < (int)n; ++i) {
     C->lru.push_back(i);
     C->lru_pos[i] = std::prev(C->lru.end());
@@ -665,6 +693,7 @@ void k3moe_cache_destroy(k3moe_cache* C) {
     cudaEventDestroy(pr.second);
   }
   for (auto e : C->free_events) cudaEventDestroy(e);
+  if (C->prefetch_done) cudaEventDestroy(C->prefetch_done);
   cudaFree(C->slots);
   cudaFreeHost(C->ring);
   cudaFree(C->d_state);
@@ -715,6 +744,98 @@ int k3moe_cache_set_device_lru(k3moe_cache* C, int enable) {
   CUDA_TRY(cudaMemset((void*)C->d_owner, 0, (size_t)n * sizeof(int32_t*)));
   CUDA_TRY(cudaMemcpy(C->d_state, &st, sizeof(st), cudaMemcpyHostToDevice));
   C->device_lru = true;
+  return K3MOE_OK;
+}
+
+int k3moe_cache_prefetch(k3moe_layer* L, const int32_t* experts, int n, int* fetched) {
+  if (fetched) *fetched = 0;
+  if (!L) return fail(K3MOE_ERR_INVALID_ARG, "layer is NULL");
+  k3moe_cache* C = L->cache;
+  if (!C) return fail(K3MOE_ERR_INVALID_ARG, "the layer has no cache: its experts are device-resident");
+  if (C->device_lru)
+    return fail(K3MOE_ERR_UNSUPPORTED, "prefetch needs the host-side LRU bookkeeping (the cache keeps it on the device)");
+  if (n < 0 || (n > 0 && !experts)) return fail(K3MOE_ERR_INVALID_ARG, "bad expert list (n=%d)", n);
+  const int E = L->dims.E;
+  for (int i = 0; i < n; ++i)
+    if (experts[i] < 0 || experts[i] >= E)
+      return fail(K3MOE_ERR_INVALID_ARG, "experts[%d]=%d is not in 0..%d", i, experts[i], E - 1);
+  // a prefetch takes a serial like a call: the slots it touches are not taken by a later prefetch
+  // before a call (or k3moe_sync) has waited for the work queued up to here
+  const long long serial = C->calls_issued++;
+  auto may_take = [&](int slot) {
+    return C->slot_key[slot] < 0 || (!C->fast_since_sync && C->slot_call[slot] < C->done_before);
+  };
+  for (int i = 0; i < n; ++i) {
+    auto it = C->where.find(((long long)L->uid << 32) | experts[i]);
+    if (it == C->where.end()) continue;
+    const int slot = it->second;
+    C->lru.erase(C->lru_pos[slot]);
+    C->lru.push_front(slot);
+    C->lru_pos[slot] = C->lru.begin();
+    C->slot_call[slot] = std::max(C->slot_call[slot], serial);
+  }
+  int got = 0;
+  int failed_e = -1;
+  cudaError_t failed_ce = cudaSuccess;
+  cudaEvent_t a = nullptr;
+  for (int i = 0; i < n; ++i) {
+    const int e = experts[i];
+    const long long key = ((long long)L->uid << 32) | e;
+    if (C->where.count(key)) continue;  // resident, or listed twice
+    const int slot = C->lru.back();
+    if (!may_take(slot)) break;  // every slot nearer the front was touched later: in flight too
+    if (!a) {
+      // the copies need no wait on a compute stream: no call in flight reads the slots they fill
+      if (!C->free_events.empty()) { a = C->free_events.back(); C->free_events.pop_back(); } else cudaEventCreate(&a);
+      CUDA_TRY(cudaEventRecord(a, C->copy_stream));
+    }
+    C->lru.pop_back();
+    if (C->slot_key[slot] >= 0) {
+      C->where.erase(C->slot_key[slot]);
+      C->st.evictions += 1;
+      C->resident[(int)(C->slot_key[slot] >> 32)] -= 1;
+    }
+    C->resident[L->uid] += 1;
+    C->slot_key[slot] = key;
+    C->where[key] = slot;
+    C->lru.push_front(slot);
+    C->lru_pos[slot] = C->lru.begin();
+    C->slot_call[slot] = serial;
+    uint8_t* dst = C->slots + (size_t)slot * C->slot_bytes;
+    const bool fake = L->test_fail_copy > 0 && --L->test_fail_copy == 0;  // failure-path test
+    const cudaError_t ce = fake ? cudaErrorInvalidValue
+                                : cudaMemcpyAsync(dst, L->pool + (size_t)e * L->exp_bytes, L->exp_bytes,
+                                                  cudaMemcpyHostToDevice, C->copy_stream);
+    if (ce != cudaSuccess) {
+      if (!fake) cudaGetLastError();
+      // forget the slot (empty, least recently used): no later call takes it for a hit
+      C->where.erase(key);
+      C->slot_key[slot] = -1;
+      C->resident[L->uid] -= 1;
+      C->lru.erase(C->lru_pos[slot]);
+      C->lru.push_back(slot);
+      C->lru_pos[slot] = std::prev(C->lru.end());
+      failed_e = e;
+      failed_ce = ce;
+      break;
+    }
+    got += 1;
+    C->st.prefetched += 1;
+    C->st.h2d_bytes += L->exp_bytes;
+  }
+  if (a) {
+    cudaEvent_t b;
+    if (!C->free_events.empty()) { b = C->free_events.back(); C->free_events.pop_back(); } else cudaEventCreate(&b);
+    CUDA_TRY(cudaEventRecord(b, C->copy_stream));
+    C->pending.emplace_back(a, b);
+    if (!C->prefetch_done) CUDA_TRY(cudaEventCreateWithFlags(&C->prefetch_done, cudaEventDisableTiming));
+    CUDA_TRY(cudaEventRecord(C->prefetch_done, C->copy_stream));
+    C->prefetch_pending = true;
+  }
+  if (fetched) *fetched = got;
+  if (failed_e >= 0)
+    return fail(K3MOE_ERR_CUDA, "prefetching expert %d into its cache slot failed: %s", failed_e,
+                cudaGetErrorString(failed_ce));
   return K3MOE_OK;
 }
 
@@ -1069,6 +1190,12 @@ int k3moe_sync(k3moe_layer* L) {
   if (!L) return fail(K3MOE_ERR_INVALID_ARG, "layer is NULL");
   if (L->last_stream) CUDA_TRY(cudaStreamSynchronize(L->last_stream));
   CUDA_TRY(cudaDeviceSynchronize());
+  if (L->cache) {
+    // every call and copy so far has finished: a prefetch may take any slot
+    L->cache->done_before = L->cache->calls_issued;
+    L->cache->fast_since_sync = false;
+    L->cache->prefetch_pending = false;
+  }
   uint32_t flags = 0;
   CUDA_TRY(cudaMemcpy(&flags, L->ws.sync + 1, 4, cudaMemcpyDeviceToHost));
   if (flags) {

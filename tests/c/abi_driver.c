@@ -39,6 +39,9 @@ int main(void) {
   CHECK(msg != NULL && strstr(msg, "d=100") != NULL, 9);
   CHECK(k3moe_cache_simulate(ref, starts, 20, 0, K3MOE_POLICY_LRU, 0, &st) == K3MOE_ERR_INVALID_ARG, 10);
   CHECK(k3moe_router_topk(NULL, w, 1, NULL, NULL, NULL) == K3MOE_ERR_INVALID_ARG, 11);
+  int fetched = -1;
+  const int32_t ids[2] = {0, 1};
+  CHECK(k3moe_cache_prefetch(NULL, ids, 2, &fetched) == K3MOE_ERR_INVALID_ARG && fetched == 0, 12);
   k3moe_layer_free(NULL);
   puts("ok");
   return 0;
