@@ -49,6 +49,27 @@ def assert_routing_matches(idx_gpu, w_gpu, idx_o, w_o, keys_o):
             assert abs(wg[e] - wo) <= 1e-5 * max(1.0, abs(wo)), f"token {t}: weight of expert {e}"
 
 
+def assert_routing_valid(idx_gpu, w_gpu, logits_o, keys_o, tol):
+    """For tokens whose k-th and (k+1)-th oracle keys may be closer than the GPU's rounding: the
+    GPU's picks are k distinct experts that form a top-k of the oracle keys within `tol` (no
+    unpicked key above a picked one by more than tol), in descending key order within tol, and
+    the weights are the oracle's sigmoid scores of the GPU's own picks, renormalised (within
+    1e-5)."""
+    T, k = idx_gpu.shape
+    E = keys_o.shape[1]
+    sig = 1.0 / (1.0 + np.exp(-logits_o))
+    for t in range(T):
+        pick = idx_gpu[t].astype(np.int64)
+        assert len(set(pick.tolist())) == k and pick.min() >= 0 and pick.max() < E, f"token {t}: bad picks"
+        rest = np.setdiff1d(np.arange(E), pick)
+        kp = keys_o[t, pick]
+        if rest.size:
+            assert kp.min() >= keys_o[t, rest].max() - tol, f"token {t}: not a top-{k} within {tol}"
+        assert (np.diff(kp) <= tol).all(), f"token {t}: slots out of key order"
+        wo = sig[t, pick] / sig[t, pick].sum()
+        assert np.abs(w_gpu[t] - wo).max() <= 1e-5, f"token {t}: weights"
+
+
 def assert_y_close(y_gpu, y_o, sumabs, what=""):
     err = np.abs(y_gpu.astype(np.float64) - y_o)
     bound = REL_TOL * sumabs + ABS_TOL

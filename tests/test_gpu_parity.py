@@ -10,7 +10,8 @@ import pytest
 
 import oracle
 import synth
-from helpers import assert_routing_matches, assert_y_close, gap_filtered_tokens, unpack_tiles
+from helpers import (GAP_MIN, assert_routing_matches, assert_routing_valid, assert_y_close, gap_filtered_tokens,
+                     unpack_tiles)
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -317,6 +318,54 @@ def test_k3_batched_decode_t64(k3_layer):
     # whole-batch invariant at any size: bitwise repeatable
     _, _, y2 = _run(layer, x)
     assert np.array_equal(y, y2)
+
+
+def _bench_check(layer, Wr, x, T, calls, n_y, what):
+    """The benchmark's own tokens (its seed and stream offset, no gap filter) in its launch
+    configuration: `calls` layer calls of T tokens.  Routing of every token against the oracle:
+    exact where the oracle's k-th/(k+1)-th key gap is at least GAP_MIN, a valid top-k within the
+    router's rounding elsewhere.  y of n_y sampled separated tokens (first and last included)
+    element by element against the oracle.  A second pass over all calls is bitwise identical."""
+    n = T * calls
+    xd = _dev(x)
+    idx = torch.empty((n, K3K), dtype=torch.int32, device="cuda")
+    w = torch.empty((n, K3K), dtype=torch.float32, device="cuda")
+    ys = [torch.empty((n, K3D), dtype=torch.float32, device="cuda") for _ in range(2)]
+    for c in range(calls):
+        sl = slice(c * T, (c + 1) * T)
+        k3.k3moe_router_topk(layer, xd[sl], T, idx[sl], w[sl])
+    for y in ys:
+        for c in range(calls):
+            sl = slice(c * T, (c + 1) * T)
+            k3.k3moe_layer_forward(layer, xd[sl], T, y[sl])
+    torch.cuda.synchronize()
+    assert torch.equal(ys[0], ys[1]), f"{what}: not bitwise repeatable"
+    idx_h, w_h, y_h = idx.cpu().numpy(), w.cpu().numpy(), ys[0].cpu().numpy()
+    i_o, w_o, lg_o, keys = oracle.router(x, Wr, None, K3K)
+    sep = oracle.topk_gap(keys, K3K) >= GAP_MIN
+    assert sep.sum() >= n // 2
+    assert_routing_matches(idx_h[sep], w_h[sep], i_o[sep], w_o[sep], keys[sep])
+    # fp32 GEMV (T < 64) or bf16 hi+lo tensor-core logits (T >= 64, error <= 4e-4 worst case)
+    assert_routing_valid(idx_h[~sep], w_h[~sep], lg_o[~sep], keys[~sep], 1e-5 if T < 64 else 5e-4)
+    cand = np.nonzero(sep)[0]
+    rng = np.random.default_rng(SEED + T)
+    sample = sorted(set(rng.choice(cand[1:-1], size=n_y - 2, replace=False).tolist()) | {int(cand[0]), int(cand[-1])})
+    y_o, sa = _k3_oracle_y(x[sample], i_o[sample], w_o[sample])
+    assert_y_close(y_h[sample], y_o, sa, f"{what}, {len(sample)} sampled tokens")
+
+
+def test_k3_benchmark_tokens_single_token_decode(k3_layer):
+    """The single-token decode benchmark's 1000 tokens, one T=1 call each."""
+    layer, Wr = k3_layer
+    x = synth.tokens_bf16(SEED, 0, 0, 1000, K3D)
+    _bench_check(layer, Wr, x, 1, 1000, 24, "K3 T=1 benchmark tokens")
+
+
+def test_k3_benchmark_tokens_batched_decode(k3_layer):
+    """The batched decode benchmark's 15 calls of 64 tokens (its stream offset in the default run)."""
+    layer, Wr = k3_layer
+    x = synth.tokens_bf16(SEED, 0, 1_000_000, 15 * 64, K3D)
+    _bench_check(layer, Wr, x, 64, 15, 16, "K3 T=64 benchmark tokens")
 
 
 def test_bounded_wait_reports_timeout_and_context_survives():
