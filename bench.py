@@ -82,6 +82,18 @@ def _peaks():
     return 6400.0, 1800.0, "fallback"
 
 
+def _bf16_sustained():
+    """The sustained (seconds-long, power-capped) bf16 rate, for work timed inside long steps."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            return json.load(fh).get("bf16_tflops_sustained", 1400.0), "measured"
+    return 1400.0, "fallback"
+
+
+NOMINAL_HBM_GBS = 8000.0  # the nominal HBM figure the layer's throughput target is stated against
+
+
 class ClockSampler:
     """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
 
@@ -303,13 +315,23 @@ def measure(torch, k3, layer, T, calls, xs, args, pg, rank, peaks):
     e2e_s = time.perf_counter() - t0
     e2e_val = job_rate_min(tokens_per_step * e2e_steps / e2e_s, pg)
     ms_step = ms / args.steps
+    bf16_sus, _ = _bf16_sustained()
+    layer_tflops = 6.0 * F * D * K * tokens_per_step * args.steps / (ms / 1e3) / 1e12
     return {
         "value": round(value, 3), "unit": "tokens/s", "ms_per_step": round(ms_step, 4),
         "calls_per_step": calls, "tokens_per_step": tokens_per_step, "us_per_call": round(1e3 * ms_step / calls, 2),
         "weight_gbs": round(weight_bytes_per_step * args.steps * (pg.get_world_size() if pg else 1)
                             / (ms / 1e3) / 1e9, 1),
         "weight_pct_of_hbm_peak": round(100 * weight_bytes_per_step * args.steps / (ms / 1e3) / 1e9 / hbm_peak, 1),
+        "weight_pct_of_nominal_8tbs": round(100 * weight_bytes_per_step * args.steps / (ms / 1e3) / 1e9
+                                            / NOMINAL_HBM_GBS, 1),
         "distinct_experts_per_call": round(distinct / calls, 2),
+        # the whole layer's expert flops (6 f d per pick: gate, up, down) over its time, against
+        # the measured bf16 peaks (burst, and sustained under the power cap)
+        "layer_tflops": round(layer_tflops, 1),
+        "layer_pct_of_bf16": {"burst": round(100 * layer_tflops / bf16_peak, 1),
+                              "sustained": round(100 * layer_tflops / bf16_sus, 1),
+                              "peak_kind": peak_kind},
         "roofline": roofline,
         "kernel_ms_per_launch": {k: round(v[0] / v[1], 5) for k, v in prof.items() if v[1]},
         "kernel_timing": f"event pairs around every launch, second pass of the same {args.steps} steps "
@@ -385,7 +407,8 @@ def run_b300(args):
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                        "l2": L2_NOTE[head_name]},
         }
-        for key in ("weight_gbs", "weight_pct_of_hbm_peak", "distinct_experts_per_call", "roofline",
+        for key in ("weight_gbs", "weight_pct_of_hbm_peak", "weight_pct_of_nominal_8tbs", "layer_tflops",
+                    "layer_pct_of_bf16", "distinct_experts_per_call", "roofline",
                     "kernel_ms_per_launch", "kernel_timing", "gpu_launches", "e2e"):
             out[key] = head[key]
         out["clocks"] = clk
