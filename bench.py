@@ -251,38 +251,55 @@ def measure(torch, k3, layer, T, calls, xs, args, pg, rank, peaks):
     y = torch.empty((tokens_per_step, D), dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
 
-    def step():
+    def step(s=None):
+        s = stream if s is None else s
         for c in range(calls):
-            k3.k3moe_layer_forward(layer, xd[c * T:(c + 1) * T], T, y[c * T:(c + 1) * T], stream)
+            k3.k3moe_layer_forward(layer, xd[c * T:(c + 1) * T], T, y[c * T:(c + 1) * T], s)
 
     for _ in range(args.warmup):
         step()
     k3.k3moe_sync(layer)
+    # Decode configurations: the step's layer calls are captured once as a CUDA graph and the
+    # timed steps replay it (a decode loop's launch overhead leaves the host; the calls and
+    # their bytes are the eager calls', which a GPU test checks).  The eager steps are timed too.
+    graph = None
+    if T < 512 and not args.eager:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=torch.cuda.Stream()):
+            step(torch.cuda.current_stream())
+        graph.replay()
+        k3.k3moe_sync(layer)
 
-    def timed(n_steps):
+    def timed(n_steps, use_graph):
         if pg:
             pg.barrier()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(n_steps):
-            step()
+            if use_graph:
+                graph.replay()
+            else:
+                step()
         e1.record(stream)
         torch.cuda.synchronize()
         if pg:
             pg.barrier()
         return e0.elapsed_time(e1)
 
-    ms = timed(args.steps)
+    ms = timed(args.steps, graph is not None)
     k3.k3moe_sync(layer)  # any device-side wait that gave up would make the timing invalid
+    ms_eager = timed(args.steps, False) if graph is not None else ms
+    k3.k3moe_sync(layer)
     # per-kernel durations: the same steps again with an event pair around every launch (the
     # events sit between kernels and stop programmatic launch overlap, so the headline timing
     # above runs without them)
     k3.k3moe_profile(layer, True)
-    ms_profiled = timed(args.steps)
+    ms_profiled = timed(args.steps, False)
     prof = k3.k3moe_profile_read(layer)
     k3.k3moe_profile(layer, False)
     value, ms = job_throughput(tokens_per_step * args.steps, ms, pg)
+    value_eager, ms_eager = job_throughput(tokens_per_step * args.steps, ms_eager, pg)
 
     # distinct experts touched (algorithmic weight bytes): counted from the actual routing
     idx = torch.empty((tokens_per_step, K), dtype=torch.int32, device="cuda")
@@ -320,6 +337,9 @@ def measure(torch, k3, layer, T, calls, xs, args, pg, rank, peaks):
     return {
         "value": round(value, 3), "unit": "tokens/s", "ms_per_step": round(ms_step, 4),
         "calls_per_step": calls, "tokens_per_step": tokens_per_step, "us_per_call": round(1e3 * ms_step / calls, 2),
+        "launch": ("one CUDA graph per step: the step's layer calls captured once, then replayed"
+                   if graph is not None else "eager layer calls"),
+        "eager": {"value": round(value_eager, 3), "ms_per_step": round(ms_eager / args.steps, 4)},
         "weight_gbs": round(weight_bytes_per_step * args.steps * (pg.get_world_size() if pg else 1)
                             / (ms / 1e3) / 1e9, 1),
         "weight_pct_of_hbm_peak": round(100 * weight_bytes_per_step * args.steps / (ms / 1e3) / 1e9 / hbm_peak, 1),
@@ -411,6 +431,8 @@ def run_b300(args):
                     "layer_pct_of_bf16", "distinct_experts_per_call", "roofline",
                     "kernel_ms_per_launch", "kernel_timing", "gpu_launches", "e2e"):
             out[key] = head[key]
+        out["config"]["launch"] = head["launch"]
+        out["eager"] = head["eager"]
         out["clocks"] = clk
         out["cpu_baseline"] = None if cpu is None else cpu[head_name]["all_cores"]
         if len(names) > 1:
@@ -762,6 +784,9 @@ def main():
                          "layer's router on this layer's input")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="decode configurations: time eager layer calls only (default: the step's calls "
+                         "replayed as one captured CUDA graph, eager timed beside it)")
     ap.add_argument("--experts", type=int, default=E,
                     help="experts resident (default 896); fewer gives a small case with the same per-call work "
                          "at T=1, for profiler captures")

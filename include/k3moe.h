@@ -195,6 +195,10 @@ int k3moe_bucket(k3moe_layer* layer, const int32_t* idx, int T, int32_t* counts,
  * In cache mode the call synchronises `stream` once (to learn which experts it needs), unless
  * every expert of the layer already sits in a slot and the cache has a slot for every expert
  * of every layer using it (then nothing can be evicted and the lookup is skipped).
+ * A device-resident layer's call only queues work on `stream` (no host synchronisation, no
+ * allocation), so it can be captured into a CUDA graph by stream capture and replayed with the
+ * same bytes, after one eager call of each path has run (that call sets the kernels' attributes);
+ * capture with per-kernel timing (k3moe_profile) off.
  * Errors: INVALID_ARG, CUDA, TIMEOUT, BUDGET_TOO_SMALL, OOM (cache mode). */
 int k3moe_layer_forward(k3moe_layer* layer, const void* x_bf16, int T, float* y, void* stream);
 
