@@ -187,7 +187,8 @@ int k3moe_bucket(k3moe_layer* layer, const int32_t* idx, int T, int32_t* counts,
  * weights -> combine ("four reductions", reduction 1; invariants row 5):
  *   y[t,:] = sum_{slot=0..k-1} w[t,slot] * W_d,e (silu(W_g,e x_t) * (W_u,e x_t)),
  *   e = idx[t,slot], silu(z) = z/(1+exp(-z)), summed in slot order.
- *   x  device pointer, [T][d] bf16 row-major, 16-byte aligned;  y  device pointer, [T][d] float32 (output).
+ *   x  device pointer, [T][d] bf16 row-major, 16-byte aligned;
+ *   y  device pointer, [T][d] float32 (output), 16-byte aligned.
  *   T  1..T_max.  y excludes any residual.
  * The result does not depend on the cache budget, on which experts were resident, or on
  * the run (bitwise).  Small T runs the register-decode path, large T the tcgen05 grouped
@@ -204,7 +205,8 @@ int k3moe_layer_forward(k3moe_layer* layer, const void* x_bf16, int T, float* y,
 
 /* k3moe_layer_forward with HOST buffers: copies x (host, [T][d] bf16) to the device, runs
  * the layer, copies y back to host ([T][d] float32) and synchronises `stream`.  Pinned host
- * memory gives the fastest copies; pageable memory also works.  Errors as layer_forward. */
+ * memory gives the fastest copies; pageable memory also works; neither needs any alignment
+ * (device staging buffers hold x and y).  Errors as layer_forward. */
 int k3moe_layer_forward_host(k3moe_layer* layer, const void* x_bf16_host, int T, float* y_host, void* stream);
 
 /* Synchronise the layer's last stream and report device-side failures: every wait inside

@@ -1154,6 +1154,8 @@ int k3moe_bucket(k3moe_layer* L, const int32_t* idx, int T, int32_t* counts, int
 int k3moe_layer_forward(k3moe_layer* L, const void* x, int T, float* y, void* stream) {
   if (!L || !x || !y) return fail(K3MOE_ERR_INVALID_ARG, "NULL argument");
   if ((reinterpret_cast<uintptr_t>(x) & 15u) != 0) return fail(K3MOE_ERR_INVALID_ARG, "x must be 16-byte aligned");
+  // the combine writes y four floats at a time
+  if ((reinterpret_cast<uintptr_t>(y) & 15u) != 0) return fail(K3MOE_ERR_INVALID_ARG, "y must be 16-byte aligned");
   if (T < 1 || T > L->dims.T_max) return fail(K3MOE_ERR_INVALID_ARG, "T=%d must be in 1..%d", T, L->dims.T_max);
   return forward_impl(L, x, T, y, reinterpret_cast<cudaStream_t>(stream));
 }

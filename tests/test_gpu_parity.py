@@ -232,9 +232,22 @@ def test_deterministic_and_host_entry_point():
     y1 = L.forward(x)
     y2 = L.forward(x)
     assert np.array_equal(y1, y2)
-    yh = np.empty((9, 512), np.float32)
+    yh = np.empty((9, 512), np.float32)  # pageable: staging buffer and a copy back
     k3.k3moe_layer_forward_host(L.layer, np.ascontiguousarray(x), 9, yh)
     assert np.array_equal(yh, y1)
+    # pinned host memory, aligned or 4 bytes off a 16-byte boundary (staging buffers hold x and y)
+    pin = torch.zeros(9 * 512 + 4, dtype=torch.float32).pin_memory()
+    for off in (0, 1):
+        yp = pin[off:off + 9 * 512].view(9, 512)
+        yp.zero_()
+        k3.k3moe_layer_forward_host(L.layer, np.ascontiguousarray(x), 9, yp)
+        assert np.array_equal(yp.numpy(), y1), f"pinned y_host at float offset {off}"
+    # a device y that is not 16-byte aligned is refused before any work is queued
+    yd = torch.zeros(9 * 512 + 4, dtype=torch.float32, device="cuda")
+    xd = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).cuda()
+    with pytest.raises(k3.K3MoEError) as ei:
+        k3.k3moe_layer_forward(L.layer, xd, 9, yd[1:1 + 9 * 512])
+    assert ei.value.code == k3.K3MOE_ERR_INVALID_ARG and "y must be 16-byte aligned" in str(ei.value)
     L.free()
 
 
