@@ -4,7 +4,8 @@
  * deleted object's fields or undefined behaviour in the argument checks, the cache simulator or
  * the expert cache's LRU bookkeeping aborts the run.
  *   Without a GPU: the cache simulator on random traces under every policy, and the refusals.
- *   With a GPU: also a layer in cache mode driven through the host-buffer entry point (hits,
+ *   With a GPU: also a layer in cache mode driven through the host-buffer entry point, with
+ *   prefetches between the calls (hits,
  *   misses, evictions, a failed copy injected on the host, a move to another cache).
  * Prints "ok cpu" (no device) or "ok gpu", exit code 0, when every check holds. */
 #include <stdint.h>
@@ -120,6 +121,16 @@ static int gpu_checks(void) {
   for (int call = 0; call < 40; ++call) {
     for (int i = 0; i < 2 * 256; ++i) x[i] = (uint16_t)(0x3c00u + (rnd() % 0x0400u) + ((rnd() & 1u) << 15));
     if (call == 20) CHECK(k3moe_set_option(layer, K3MOE_OPT_TEST_FAIL_COPY, 1) == K3MOE_OK, 302);
+    if ((call & 1) && call < 30) { /* prefetch three experts (repeats allowed) before the call */
+      int32_t ids[3];
+      for (int j = 0; j < 3; ++j) ids[j] = (int32_t)(rnd() % (uint32_t)dm.E);
+      int got = -1;
+      const int prc = k3moe_cache_prefetch(layer, ids, 3, &got);
+      if (prc == K3MOE_ERR_CUDA && call >= 20 && !failed)
+        failed = 1; /* the injected copy failure came in a prefetch */
+      else
+        CHECK(prc == K3MOE_OK && got >= 0 && got <= 3, 309);
+    }
     const int rc = k3moe_layer_forward_host(layer, x, 2, y, NULL);
     if (rc == K3MOE_ERR_CUDA && call >= 20 && !failed) {
       failed = 1; /* the injected copy failure (a call that needed a copy) */
@@ -132,6 +143,9 @@ static int gpu_checks(void) {
   k3moe_cache_stats_t st1, st2;
   CHECK(k3moe_cache_stats(c1, &st1) == K3MOE_OK && k3moe_cache_stats(c2, &st2) == K3MOE_OK, 306);
   CHECK(st1.misses > 0 && st1.evictions > 0 && st2.misses > 0, 307);
+  CHECK(st1.prefetched > 0 && st1.h2d_bytes == (st1.misses + st1.prefetched) * eb, 310);
+  int32_t bad = dm.E;
+  CHECK(k3moe_cache_prefetch(layer, &bad, 1, NULL) == K3MOE_ERR_INVALID_ARG, 311);
   CHECK(k3moe_cache_reset_stats(c2) == K3MOE_OK, 308);
   k3moe_layer_free(layer);
   k3moe_cache_destroy(c1);
