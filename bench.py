@@ -73,6 +73,26 @@ def _dist():
     return ws, rank
 
 
+def _set_ffn_width(f):
+    """Expert sizes for an FFN width other than K3's (profiling cases): 17/32 bytes per weight."""
+    global F, EXPERT_BYTES, GATEUP_BYTES, DOWN_BYTES
+    if f <= 0 or f % 128:
+        raise SystemExit("--f must be a positive multiple of 128")
+    F = f
+    DOWN_BYTES = f * D * 17 // 32
+    GATEUP_BYTES = 2 * DOWN_BYTES
+    EXPERT_BYTES = 3 * DOWN_BYTES
+
+
+def _profiling_case(args):
+    parts = []
+    if args.experts != E:
+        parts.append(f"only {args.experts} experts resident")
+    if args.f != 1536:
+        parts.append(f"f={args.f}")
+    return f" [profiling case: {', '.join(parts)}]" if parts else ""
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -420,9 +440,7 @@ def run_b300(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "mxfp4 weights -> f16 mma, f32 accumulate",
             "data": "synthetic (seeded splitmix64 experts, N(0,1) bf16 tokens, N(0,1/d) router)",
             "impl": "b300",
-            "config": {"workload": WORKLOADS[head_name]["desc"] + ("" if args.experts == E else
-                                                                   f" [profiling case: only {args.experts} "
-                                                                   f"experts resident]"),
+            "config": {"workload": WORKLOADS[head_name]["desc"] + _profiling_case(args),
                        "calls_per_step": head["calls_per_step"], "tokens_per_step": head["tokens_per_step"],
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                        "l2": L2_NOTE[head_name]},
@@ -790,7 +808,12 @@ def main():
     ap.add_argument("--experts", type=int, default=E,
                     help="experts resident (default 896); fewer gives a small case with the same per-call work "
                          "at T=1, for profiler captures")
+    ap.add_argument("--f", type=int, default=F,
+                    help="expert intermediate width (default 1536, a multiple of 128); a narrow FFN gives a "
+                         "small case in which the router still does the full layer's work, for profiler captures")
     args = ap.parse_args()
+    if args.f != F:
+        _set_ffn_width(args.f)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.prefetch != "none" and args.device_lru:
