@@ -17,8 +17,7 @@ constexpr size_t kMcChunk = (size_t)kMcThreads * kMcUnroll * 16 * 4;   // 64 KB 
 
 // CTA b copies chunks b, b + gridDim.x, ... of the concatenation of the n missed experts
 // (`bytes` each, a multiple of 16; both addresses 16-byte aligned).
-__global__ void __launch_bounds__(kMcThreads) miss_copy_kernel(const MissCopy* __restrict__ list, int n,
-                                                               size_t bytes) {
+__device__ __forceinline__ void copy_misses(const MissCopy* __restrict__ list, int n, size_t bytes) {
   const size_t per = (bytes + kMcChunk - 1) / kMcChunk;
   const size_t total = per * (size_t)n;
   for (size_t c = blockIdx.x; c < total; c += gridDim.x) {
@@ -41,6 +40,12 @@ __global__ void __launch_bounds__(kMcThreads) miss_copy_kernel(const MissCopy* _
       }
     }
   }
+}
+
+// The miss list and its count come from the host bookkeeping (kernel arguments).
+__global__ void __launch_bounds__(kMcThreads) miss_copy_kernel(const MissCopy* __restrict__ list, int n,
+                                                               size_t bytes) {
+  copy_misses(list, n, bytes);
 }
 
 }  // namespace
@@ -138,33 +143,11 @@ __global__ void lru_detach_kernel(LruState* st, int32_t* prev, int32_t* next, in
   }
 }
 
-// The copy kernel for a miss count that lives on the device (at most max_n).
+// The copy kernel for a miss list and count written on the device by the lookup kernel.
 __global__ void __launch_bounds__(kMcThreads) miss_copy_dev_kernel(const MissCopy* __restrict__ list,
                                                                    const int32_t* n_dev, size_t bytes) {
   pdl_entry();
-  const int n = *n_dev;
-  const size_t per = (bytes + kMcChunk - 1) / kMcChunk;
-  const size_t total = per * (size_t)n;
-  for (size_t c = blockIdx.x; c < total; c += gridDim.x) {
-    const int m = (int)(c / per);
-    const size_t base = (c % per) * kMcChunk;
-    const uint4* src = reinterpret_cast<const uint4*>(list[m].src + base);
-    uint4* dst = reinterpret_cast<uint4*>(list[m].dst + base);
-    const size_t words = (bytes - base < kMcChunk ? bytes - base : kMcChunk) / 16;
-    for (size_t w0 = threadIdx.x; w0 < words; w0 += (size_t)kMcThreads * kMcUnroll) {
-      uint4 v[kMcUnroll];
-#pragma unroll
-      for (int u = 0; u < kMcUnroll; ++u) {
-        const size_t w = w0 + (size_t)u * kMcThreads;
-        if (w < words) v[u] = src[w];
-      }
-#pragma unroll
-      for (int u = 0; u < kMcUnroll; ++u) {
-        const size_t w = w0 + (size_t)u * kMcThreads;
-        if (w < words) dst[w] = v[u];
-      }
-    }
-  }
+  copy_misses(list, *n_dev, bytes);
 }
 
 }  // namespace
