@@ -224,6 +224,32 @@ cudaError_t fold_ring(k3moe_cache* C) {
   return cudaSuccess;
 }
 
+// A timing event for the cache's copies: one from the pool, else a new one.
+cudaEvent_t cache_event(k3moe_cache* C) {
+  cudaEvent_t e = nullptr;
+  if (!C->free_events.empty()) {
+    e = C->free_events.back();
+    C->free_events.pop_back();
+  } else {
+    cudaEventCreate(&e);
+  }
+  return e;
+}
+
+// The slot holds no valid expert (any more): it becomes empty and least recently used, so that
+// no later call takes it for a hit and the next miss takes it first.
+void forget_slot(k3moe_cache* C, int slot) {
+  const long long key = C->slot_key[slot];
+  if (key >= 0) {
+    C->where.erase(key);
+    C->resident[(int)(key >> 32)] -= 1;
+  }
+  C->slot_key[slot] = -1;
+  C->lru.erase(C->lru_pos[slot]);
+  C->lru.push_back(slot);
+  C->lru_pos[slot] = std::prev(C->lru.end());
+}
+
 int attach_cache(k3moe_layer* L, k3moe_cache* C) {
   if (C->device_lru) {
     // the lookup kernel cannot refuse a call: every call must fit in the slots
@@ -256,16 +282,9 @@ void detach_cache(k3moe_layer* L) {
   }
   fold_ring(C);
   C->experts_attached -= L->dims.E;
+  for (int s = 0; s < C->n_slots; ++s)
+    if (C->slot_key[s] >= 0 && (int)(C->slot_key[s] >> 32) == L->uid) forget_slot(C, s);
   C->resident.erase(L->uid);
-  for (int s = 0; s < C->n_slots; ++s) {
-    if (C->slot_key[s] >= 0 && (int)(C->slot_key[s] >> 32) == L->uid) {
-      C->where.erase(C->slot_key[s]);
-      C->slot_key[s] = -1;
-      C->lru.erase(C->lru_pos[s]);
-      C->lru.push_back(s);
-      C->lru_pos[s] = std::prev(C->lru.end());
-    }
-  }
   C->users -= 1;
   L->cache = nullptr;
 }
@@ -358,9 +377,7 @@ int make_resident(k3moe_layer* L, cudaStream_t s) {
     LruArgs la{C->d_state, C->d_prev, C->d_next, C->d_owner, C->n_slots, C->slots, C->slot_bytes, L->ws.act,
                L->ws.nact, L->d_slot_of, (const uint8_t**)L->eptr_dev, L->pool_dev, L->miss_dev, L->d_nmiss,
                L->ws.sync + 1};
-    cudaEvent_t a, b;
-    if (!C->free_events.empty()) { a = C->free_events.back(); C->free_events.pop_back(); } else cudaEventCreate(&a);
-    if (!C->free_events.empty()) { b = C->free_events.back(); C->free_events.pop_back(); } else cudaEventCreate(&b);
+    cudaEvent_t a = cache_event(C), b = cache_event(C);
     CUDA_TRY(launch_lru_lookup(la, s));
     CUDA_TRY(cudaEventRecord(a, s));
     CUDA_TRY(launch_miss_copy_dev(L->miss_dev, L->d_nmiss, std::min(E, L->dims.T_max * L->dims.k), L->exp_bytes,
@@ -418,9 +435,7 @@ int make_resident(k3moe_layer* L, cudaStream_t s) {
     }
   }
   if (!miss.empty()) {
-    cudaEvent_t a, b;
-    if (!C->free_events.empty()) { a = C->free_events.back(); C->free_events.pop_back(); } else cudaEventCreate(&a);
-    if (!C->free_events.empty()) { b = C->free_events.back(); C->free_events.pop_back(); } else cudaEventCreate(&b);
+    cudaEvent_t a = cache_event(C), b = cache_event(C);
     const bool zc = L->miss_path == K3MOE_MISS_ZERO_COPY;
     if (zc) {
       // the copy kernel runs on `s` itself, after every earlier use of the slots on `s`
@@ -461,15 +476,9 @@ int make_resident(k3moe_layer* L, cudaStream_t s) {
                              C->copy_stream);
       if (ce != cudaSuccess) {
         if (!fake) cudaGetLastError();
-        // the slot holds no valid expert: forget it (empty, least recently used) so that no later
-        // call takes it for a hit; the copies issued before it still complete, and later work on
-        // `s` is ordered after them
-        C->where.erase(key);
-        C->slot_key[slot] = -1;
-        C->resident[L->uid] -= 1;
-        C->lru.erase(C->lru_pos[slot]);
-        C->lru.push_back(slot);
-        C->lru_pos[slot] = std::prev(C->lru.end());
+        // the slot holds no valid expert: forget it; the copies issued before it still complete,
+        // and later work on `s` is ordered after them
+        forget_slot(C, slot);
         failed_e = e;
         failed_ce = ce;
         break;
@@ -487,15 +496,7 @@ int make_resident(k3moe_layer* L, cudaStream_t s) {
       if (ke != cudaSuccess) {
         cudaGetLastError();
         // none of this call's slots was filled: forget them all
-        for (int i = 0; i < nm; ++i) {
-          const int slot = (int)((L->miss_host[i].dst - C->slots) / C->slot_bytes);
-          C->where.erase(C->slot_key[slot]);
-          C->slot_key[slot] = -1;
-          C->resident[L->uid] -= 1;
-          C->lru.erase(C->lru_pos[slot]);
-          C->lru.push_back(slot);
-          C->lru_pos[slot] = std::prev(C->lru.end());
-        }
+        for (int i = 0; i < nm; ++i) forget_slot(C, (int)((L->miss_host[i].dst - C->slots) / C->slot_bytes));
         return fail(K3MOE_ERR_CUDA, "zero-copy miss kernel: %s", cudaGetErrorString(ke));
       }
     } else {
@@ -786,7 +787,7 @@ int k3moe_cache_prefetch(k3moe_layer* L, const int32_t* experts, int n, int* fet
     if (!may_take(slot)) break;  // every slot nearer the front was touched later: in flight too
     if (!a) {
       // the copies need no wait on a compute stream: no call in flight reads the slots they fill
-      if (!C->free_events.empty()) { a = C->free_events.back(); C->free_events.pop_back(); } else cudaEventCreate(&a);
+      a = cache_event(C);
       CUDA_TRY(cudaEventRecord(a, C->copy_stream));
     }
     C->lru.pop_back();
@@ -808,13 +809,7 @@ int k3moe_cache_prefetch(k3moe_layer* L, const int32_t* experts, int n, int* fet
                                                   cudaMemcpyHostToDevice, C->copy_stream);
     if (ce != cudaSuccess) {
       if (!fake) cudaGetLastError();
-      // forget the slot (empty, least recently used): no later call takes it for a hit
-      C->where.erase(key);
-      C->slot_key[slot] = -1;
-      C->resident[L->uid] -= 1;
-      C->lru.erase(C->lru_pos[slot]);
-      C->lru.push_back(slot);
-      C->lru_pos[slot] = std::prev(C->lru.end());
+      forget_slot(C, slot);
       failed_e = e;
       failed_ce = ce;
       break;
@@ -824,8 +819,7 @@ int k3moe_cache_prefetch(k3moe_layer* L, const int32_t* experts, int n, int* fet
     C->st.h2d_bytes += L->exp_bytes;
   }
   if (a) {
-    cudaEvent_t b;
-    if (!C->free_events.empty()) { b = C->free_events.back(); C->free_events.pop_back(); } else cudaEventCreate(&b);
+    cudaEvent_t b = cache_event(C);
     CUDA_TRY(cudaEventRecord(b, C->copy_stream));
     C->pending.emplace_back(a, b);
     if (!C->prefetch_done) CUDA_TRY(cudaEventCreateWithFlags(&C->prefetch_done, cudaEventDisableTiming));
