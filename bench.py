@@ -230,6 +230,12 @@ def build_layer(torch, k3, T_max, bias=None, n_exp=E):
     return layer
 
 
+def _combine_gbs(prof, T):
+    """The combine kernel's HBM rate: T*k per-pick fp32 rows read, T fp32 rows of y written."""
+    ms, n = prof["combine"]
+    return round((T * K * D * 4 + T * D * 4) / (ms / n / 1e3) / 1e9, 1) if n else None
+
+
 def _roofline(prof, T, distinct_per_call, hbm_peak, bf16_peak, peak_kind):
     """Roofline of the dominant kernel from the event-timed pass: the gate/up GEMM (tensor
     bound) on the tensor-core path, the gate/up streaming kernel (HBM bound) otherwise."""
@@ -245,7 +251,8 @@ def _roofline(prof, T, distinct_per_call, hbm_peak, bf16_peak, peak_kind):
                 "algorithmic_flops_per_launch": flops,
                 "traffic": _traffic_from_profile("mxfp4_routed_expert_06_b300/csrc/gemm_tc.cu",
                                                  "gemm_gu_prefill_k3_t4096.txt") if T == 4096 else None,
-                "down_gemm_tflops": round(2.0 * F * D * T * K / (dn_ms / dn_n / 1e3) / 1e12, 1)}
+                "down_gemm_tflops": round(2.0 * F * D * T * K / (dn_ms / dn_n / 1e3) / 1e12, 1),
+                "combine_kernel_gbs": _combine_gbs(prof, T)}
     gu_ms, gu_n = prof["gateup"]
     gu_bytes = distinct_per_call * GATEUP_BYTES  # each active expert's gate/up bytes once per call
     achieved = gu_bytes / (gu_ms / gu_n / 1e3) / 1e9 if gu_n else None
@@ -258,7 +265,8 @@ def _roofline(prof, T, distinct_per_call, hbm_peak, bf16_peak, peak_kind):
             "frac": None if achieved is None else round(achieved / hbm_peak, 4),
             "peak_kind": f"{peak_kind} (HBM copy peak)",
             "algorithmic_bytes_per_launch": int(gu_bytes), "traffic": traffic,
-            "down_kernel_gbs": round(distinct_per_call * DOWN_BYTES / (dn_ms / dn_n / 1e3) / 1e9, 1) if dn_n else None}
+            "down_kernel_gbs": round(distinct_per_call * DOWN_BYTES / (dn_ms / dn_n / 1e3) / 1e9, 1) if dn_n else None,
+            "combine_kernel_gbs": _combine_gbs(prof, T)}
 
 
 def measure(torch, k3, layer, T, calls, xs, args, pg, rank, peaks):
