@@ -279,23 +279,21 @@ def measure(torch, k3, layer, T, calls, xs, args, pg, rank, peaks):
     y = torch.empty((tokens_per_step, D), dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
 
-    def step(s=None):
-        s = stream if s is None else s
+    def step():
         for c in range(calls):
-            k3.k3moe_layer_forward(layer, xd[c * T:(c + 1) * T], T, y[c * T:(c + 1) * T], s)
+            k3.k3moe_layer_forward(layer, xd[c * T:(c + 1) * T], T, y[c * T:(c + 1) * T], stream)
 
     for _ in range(args.warmup):
         step()
     k3.k3moe_sync(layer)
-    # Decode configurations: the step's layer calls are captured once as a CUDA graph and the
-    # timed steps replay it (a decode loop's launch overhead leaves the host; the calls and
-    # their bytes are the eager calls', which a GPU test checks).  The eager steps are timed too.
+    # Decode configurations: the step's layer calls are captured once as a CUDA graph by the
+    # library (k3moe_graph_create) and the timed steps replay it (a decode loop's launch overhead
+    # leaves the host; the calls and their bytes are the eager calls', which a GPU test checks).
+    # The eager steps are timed too.
     graph = None
     if T < 512 and not args.eager:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=torch.cuda.Stream()):
-            step(torch.cuda.current_stream())
-        graph.replay()
+        graph = k3.k3moe_graph_create(layer, xd, T, calls, y, stream)
+        k3.k3moe_graph_launch(graph, stream)
         k3.k3moe_sync(layer)
 
     def timed(n_steps, use_graph):
@@ -306,7 +304,7 @@ def measure(torch, k3, layer, T, calls, xs, args, pg, rank, peaks):
         e0.record(stream)
         for _ in range(n_steps):
             if use_graph:
-                graph.replay()
+                k3.k3moe_graph_launch(graph, stream)
             else:
                 step()
         e1.record(stream)
@@ -319,6 +317,8 @@ def measure(torch, k3, layer, T, calls, xs, args, pg, rank, peaks):
     k3.k3moe_sync(layer)  # any device-side wait that gave up would make the timing invalid
     ms_eager = timed(args.steps, False) if graph is not None else ms
     k3.k3moe_sync(layer)
+    if graph is not None:
+        k3.k3moe_graph_destroy(graph)
     # per-kernel durations: the same steps again with an event pair around every launch (the
     # events sit between kernels and stop programmatic launch overlap, so the headline timing
     # above runs without them)
@@ -365,8 +365,8 @@ def measure(torch, k3, layer, T, calls, xs, args, pg, rank, peaks):
     return {
         "value": round(value, 3), "unit": "tokens/s", "ms_per_step": round(ms_step, 4),
         "calls_per_step": calls, "tokens_per_step": tokens_per_step, "us_per_call": round(1e3 * ms_step / calls, 2),
-        "launch": ("one CUDA graph per step: the step's layer calls captured once, then replayed"
-                   if graph is not None else "eager layer calls"),
+        "launch": ("one CUDA graph per step: the step's layer calls captured once by k3moe_graph_create, "
+                   "then replayed with k3moe_graph_launch" if graph is not None else "eager layer calls"),
         "eager": {"value": round(value_eager, 3), "ms_per_step": round(ms_eager / args.steps, 4)},
         "weight_gbs": round(weight_bytes_per_step * args.steps * (pg.get_world_size() if pg else 1)
                             / (ms / 1e3) / 1e9, 1),

@@ -209,6 +209,26 @@ int k3moe_layer_forward(k3moe_layer* layer, const void* x_bf16, int T, float* y,
  * (device staging buffers hold x and y).  Errors as layer_forward. */
 int k3moe_layer_forward_host(k3moe_layer* layer, const void* x_bf16_host, int T, float* y_host, void* stream);
 
+/* Repeated layer calls as one CUDA graph (a decode loop's launch overhead leaves the host).
+ * k3moe_graph_create runs `calls` layer calls of T tokens once, eagerly on `stream` (call c reads
+ * x + c*T*d bf16 values and writes y + c*T*d floats, as k3moe_layer_forward does; the eager run
+ * also sets the kernels' launch attributes), then captures the same calls on a private stream
+ * into a graph.  k3moe_graph_launch replays them on `stream` with the same bytes; inputs are read
+ * and outputs written at the addresses given at creation.  k3moe_sync reports device-side
+ * failures of replayed calls as of eager ones.
+ *   layer   device-resident (packed without a cache: cache-mode calls synchronise the host),
+ *           per-kernel timing (k3moe_profile) off
+ *   x, y    device pointers, 16-byte aligned, [calls*T][d] bf16 and [calls*T][d] float32
+ *   T       1..T_max;  calls >= 1
+ * The graph holds the layer's workspace: replays of graphs of one layer, and its other calls,
+ * must be ordered (one stream).  Destroy it before the layer.
+ * Errors: INVALID_ARG, UNSUPPORTED (cache mode), CUDA, OOM, and those of k3moe_layer_forward. */
+typedef struct k3moe_graph k3moe_graph;
+int k3moe_graph_create(k3moe_layer* layer, const void* x_bf16, int T, int calls, float* y, void* stream,
+                       k3moe_graph** out);
+int k3moe_graph_launch(k3moe_graph* graph, void* stream);
+void k3moe_graph_destroy(k3moe_graph* graph);
+
 /* Synchronise the layer's last stream and report device-side failures: every wait inside
  * the kernels is bounded (K3MOE_OPT_DEVICE_WAIT_NS, default 2 s); a wait that gives up sets a
  * device flag and its kernel returns early.  This call returns K3MOE_ERR_TIMEOUT (and clears the

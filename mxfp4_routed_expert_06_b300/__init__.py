@@ -74,6 +74,9 @@ _SIGS = {
     "k3moe_bucket": ([_vp, _vp, _i, _vp, _vp, _vp, _vp], _i),
     "k3moe_layer_forward": ([_vp, _vp, _i, _vp, _vp], _i),
     "k3moe_layer_forward_host": ([_vp, _vp, _i, _vp, _vp], _i),
+    "k3moe_graph_create": ([_vp, _vp, _i, _i, _vp, _vp, ctypes.POINTER(_vp)], _i),
+    "k3moe_graph_launch": ([_vp, _vp], _i),
+    "k3moe_graph_destroy": ([_vp], None),
     "k3moe_set_option": ([_vp, _i, ctypes.c_longlong], _i),
     "k3moe_sync": ([_vp], _i),
     "k3moe_profile": ([_vp, _i], _i),
@@ -237,6 +240,22 @@ def k3moe_layer_free(layer) -> None:
 def k3moe_router_topk_noalloc(x, W_r, bias, T: int, d: int, E: int, k: int, idx, w, stream=None) -> None:
     _check(_lib.k3moe_router_topk_noalloc(_ptr(x), _ptr(W_r), _ptr(bias), T, d, E, k, _ptr(idx), _ptr(w),
                                           _stream(stream)))
+
+
+def k3moe_graph_create(layer, x, T: int, calls: int, y, stream=None):
+    """`calls` layer calls of T tokens (x, y contiguous over the calls) run once and captured as one
+    CUDA graph; returns its handle for k3moe_graph_launch."""
+    out = ctypes.c_void_p()
+    _check(_lib.k3moe_graph_create(_handle(layer), _ptr(x), T, calls, _ptr(y), _stream(stream), ctypes.byref(out)))
+    return out
+
+
+def k3moe_graph_launch(graph, stream=None) -> None:
+    _check(_lib.k3moe_graph_launch(_handle(graph), _stream(stream)))
+
+
+def k3moe_graph_destroy(graph) -> None:
+    _lib.k3moe_graph_destroy(_handle(graph))
 
 
 def k3moe_cache_create(budget_bytes: int, slot_bytes: int):

@@ -105,6 +105,13 @@ struct k3moe_cache {
   bool prefetch_pending = false;
 };
 
+// Repeated layer calls captured as one CUDA graph (k3moe_graph_create).
+struct k3moe_graph {
+  k3moe_layer* layer = nullptr;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+};
+
 struct k3moe_layer {
   k3moe_dims dims{};
   size_t exp_bytes = 0;
@@ -1180,6 +1187,67 @@ int k3moe_layer_forward_host(k3moe_layer* L, const void* x_host, int T, float* y
     return fail(K3MOE_ERR_TIMEOUT, "a device-side wait gave up (flags 0x%x)", flags);
   }
   return K3MOE_OK;
+}
+
+int k3moe_graph_create(k3moe_layer* L, const void* x, int T, int calls, float* y, void* stream, k3moe_graph** out) {
+  if (!out) return fail(K3MOE_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!L || !x || !y) return fail(K3MOE_ERR_INVALID_ARG, "NULL argument");
+  if (calls < 1) return fail(K3MOE_ERR_INVALID_ARG, "calls=%d must be at least 1", calls);
+  if (T < 1 || T > L->dims.T_max) return fail(K3MOE_ERR_INVALID_ARG, "T=%d must be in 1..%d", T, L->dims.T_max);
+  if ((reinterpret_cast<uintptr_t>(x) & 15u) != 0 || (reinterpret_cast<uintptr_t>(y) & 15u) != 0)
+    return fail(K3MOE_ERR_INVALID_ARG, "x and y must be 16-byte aligned");
+  if (L->cache)
+    return fail(K3MOE_ERR_UNSUPPORTED, "a cache-mode layer's calls synchronise the host and cannot be captured");
+  if (L->profiling) return fail(K3MOE_ERR_INVALID_ARG, "per-kernel timing is on: turn k3moe_profile off to capture");
+  const size_t xs = (size_t)T * L->dims.d * 2;  // bytes of one call's x
+  const size_t ys = (size_t)T * L->dims.d;      // floats of one call's y
+  const uint8_t* xb = static_cast<const uint8_t*>(x);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // eager once: checks the calls and sets every kernel's launch attributes outside the capture
+  for (int c = 0; c < calls; ++c) {
+    const int rc = forward_impl(L, xb + c * xs, T, y + c * ys, s);
+    if (rc) return rc;
+  }
+  // capture on a private stream (the caller's may be the legacy stream, which cannot capture)
+  cudaStream_t cs = nullptr;
+  CUDA_TRY(cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking));
+  cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+  int rc = K3MOE_OK;
+  for (int c = 0; c < calls && e == cudaSuccess && rc == K3MOE_OK; ++c) rc = forward_impl(L, xb + c * xs, T, y + c * ys, cs);
+  cudaGraph_t g = nullptr;
+  const cudaError_t e2 = e == cudaSuccess ? cudaStreamEndCapture(cs, &g) : e;
+  L->last_stream = s;
+  cudaStreamDestroy(cs);
+  if (rc != K3MOE_OK || e2 != cudaSuccess) {
+    if (g) cudaGraphDestroy(g);
+    cudaGetLastError();
+    return rc != K3MOE_OK ? rc : fail(K3MOE_ERR_CUDA, "capturing the layer calls failed: %s", cudaGetErrorString(e2));
+  }
+  cudaGraphExec_t ex = nullptr;
+  e = cudaGraphInstantiate(&ex, g, 0);
+  if (e != cudaSuccess) {
+    cudaGraphDestroy(g);
+    cudaGetLastError();
+    return fail(K3MOE_ERR_CUDA, "instantiating the captured calls failed: %s", cudaGetErrorString(e));
+  }
+  *out = new k3moe_graph{L, g, ex};
+  return K3MOE_OK;
+}
+
+int k3moe_graph_launch(k3moe_graph* G, void* stream) {
+  if (!G) return fail(K3MOE_ERR_INVALID_ARG, "graph is NULL");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  G->layer->last_stream = s;  // k3moe_sync waits for the replay here
+  CUDA_TRY(cudaGraphLaunch(G->exec, s));
+  return K3MOE_OK;
+}
+
+void k3moe_graph_destroy(k3moe_graph* G) {
+  if (!G) return;
+  if (G->exec) cudaGraphExecDestroy(G->exec);
+  if (G->graph) cudaGraphDestroy(G->graph);
+  delete G;
 }
 
 int k3moe_sync(k3moe_layer* L) {
