@@ -42,6 +42,10 @@ int main(void) {
   int fetched = -1;
   const int32_t ids[2] = {0, 1};
   CHECK(k3moe_cache_prefetch(NULL, ids, 2, &fetched) == K3MOE_ERR_INVALID_ARG && fetched == 0, 12);
+  k3moe_graph* graph = (k3moe_graph*)&fetched; /* must be cleared on refusal */
+  CHECK(k3moe_graph_create(NULL, w, 1, 1, (float*)w, NULL, &graph) == K3MOE_ERR_INVALID_ARG && graph == NULL, 13);
+  CHECK(k3moe_graph_launch(NULL, NULL) == K3MOE_ERR_INVALID_ARG, 14);
+  k3moe_graph_destroy(NULL);
   k3moe_layer_free(NULL);
   puts("ok");
   return 0;
