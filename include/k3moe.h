@@ -51,7 +51,7 @@ extern "C" {
 #define K3MOE_ERR_CUDA (-3)             /* a CUDA runtime call or kernel launch failed */
 #define K3MOE_ERR_TIMEOUT (-4)          /* a bounded device-side wait gave up */
 #define K3MOE_ERR_BUDGET_TOO_SMALL (-5) /* the cache cannot hold the experts one call needs */
-#define K3MOE_ERR_UNSUPPORTED (-6)      /* valid request this build does not implement */
+#define K3MOE_ERR_UNSUPPORTED (-6)      /* a valid request the library does not serve */
 
 /* Layer dimensions, validated strictly (unknown or inconsistent values are refused, never
  * defaulted -- the engine's strict config loading, "what you learn", last paragraph):
