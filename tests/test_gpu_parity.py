@@ -5,6 +5,8 @@ Routing (top-k sets) and bucketing must match exactly; y must be within
 Small configurations span several tiles and ragged token counts; the full Kimi K3
 shape (d=7168, f=1536, E=896, k=16) is checked on sampled tokens.
 """
+import os
+
 import numpy as np
 import pytest
 
@@ -372,6 +374,47 @@ def test_k3_benchmark_tokens_single_token_decode(k3_layer):
     layer, Wr = k3_layer
     x = synth.tokens_bf16(SEED, 0, 0, 1000, K3D)
     _bench_check(layer, Wr, x, 1, 1000, 24, "K3 T=1 benchmark tokens")
+
+
+@pytest.mark.skipif(os.environ.get("K3MOE_ORACLE_ALL") != "1",
+                    reason="opt-in (K3MOE_ORACLE_ALL=1): every token through the oracle, about 15 minutes")
+def test_k3_benchmark_tokens_every_output(k3_layer):
+    """The single-token decode benchmark's 1000 tokens, every y element against the oracle.  A token
+    whose 16th/17th oracle keys lie within GAP_MIN is checked on the GPU's own picks (a valid top-k,
+    checked as such) with the oracle's fp64 weights for them; the others on the oracle's routing."""
+    layer, Wr = k3_layer
+    n = 1000
+    x = synth.tokens_bf16(SEED, 0, 0, n, K3D)
+    xd = _dev(x)
+    y = torch.empty((n, K3D), dtype=torch.float32, device="cuda")
+    idx = torch.empty((n, K3K), dtype=torch.int32, device="cuda")
+    w = torch.empty((n, K3K), dtype=torch.float32, device="cuda")
+    for t in range(n):
+        k3.k3moe_router_topk(layer, xd[t:t + 1], 1, idx[t:t + 1], w[t:t + 1])
+        k3.k3moe_layer_forward(layer, xd[t:t + 1], 1, y[t:t + 1])
+    torch.cuda.synchronize()
+    y_h, idx_h, w_h = y.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy()
+    i_o, w_o, lg_o, keys = oracle.router(x, Wr, None, K3K)
+    sep = oracle.topk_gap(keys, K3K) >= GAP_MIN
+    assert_routing_matches(idx_h[sep], w_h[sep], i_o[sep], w_o[sep], keys[sep])
+    assert_routing_valid(idx_h[~sep], w_h[~sep], lg_o[~sep], keys[~sep], 1e-5)
+    # the picks each token is checked on, with fp64 weights for them
+    sig = 1.0 / (1.0 + np.exp(-lg_o))
+    picks = np.where(sep[:, None], i_o, idx_h)
+    wts = np.take_along_axis(sig, picks.astype(np.int64), axis=1)
+    wts = wts / wts.sum(axis=1, keepdims=True)
+    cache = {}
+    for b0 in range(0, n, 50):
+        ts = np.arange(b0, min(n, b0 + 50))
+        nibs, scls = [], []
+        for e in picks[ts].reshape(-1).tolist():
+            if e not in cache:
+                n_, s_ = synth.experts(SEED, 0, e, e + 1, K3D, K3F)
+                cache[e] = (n_[0], s_[0])
+            nibs.append(cache[e][0])
+            scls.append(cache[e][1])
+        y_o, sa = oracle.moe(x[ts], wts[ts], nibs, scls, K3F)
+        assert_y_close(y_h[ts], y_o, sa, f"K3 T=1 benchmark tokens {b0}..{ts[-1]}")
 
 
 def test_k3_benchmark_tokens_batched_decode(k3_layer):
