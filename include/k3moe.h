@@ -27,6 +27,10 @@
  *     allocates: packed weights, workspace, cache slots, pinned pools.
  *   - One layer object must not be used from two streams at the same time: calls share its
  *     workspace.  Different layer objects are independent (a shared cache excepted).
+ *   - Device buffers are aligned at least to their element size (int32 and float32: 4 bytes,
+ *     bf16: 2 bytes); x of the router and of the layer forward, and y of the layer forward, to
+ *     16 bytes.  A misaligned device pointer is refused with INVALID_ARG (a misaligned access
+ *     would be a device fault).  Host buffers of the host-buffer entry point need no alignment.
  *   - Canonical MXFP4 input layout, per expert e (experts back to back):
  *       nibbles  [3][rows][cols/2] bytes: matrix 0 = gate W_g [f][d], 1 = up W_u [f][d],
  *                2 = down W_d [d][f]; element 2i of a row in the LOW nibble of byte i;

@@ -1098,6 +1098,8 @@ void k3moe_layer_free(k3moe_layer* L) { free_layer(L); }
 int k3moe_residual_rmsnorm(const float* y, const void* x, int T, int d, float eps, void* x_next, void* x_norm,
                            void* stream) {
   if (!y || !x || !x_next || !x_norm) return fail(K3MOE_ERR_INVALID_ARG, "NULL argument");
+  if (!aligned_to(y, 4) || !aligned_to(x, 2) || !aligned_to(x_next, 2) || !aligned_to(x_norm, 2))
+    return fail(K3MOE_ERR_INVALID_ARG, "y must be 4-byte and x, x_next, x_norm 2-byte aligned");
   if (T < 1 || d < 1 || d > 65536) return fail(K3MOE_ERR_INVALID_ARG, "T=%d, d=%d out of range", T, d);
   if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(K3MOE_ERR_INVALID_ARG, "eps must be finite and >= 0");
   if (x_norm == x_next) return fail(K3MOE_ERR_INVALID_ARG, "x_norm must not alias x_next");
@@ -1128,6 +1130,7 @@ int k3moe_layer_set_cache(k3moe_layer* L, k3moe_cache* C) {
 int k3moe_router_topk(k3moe_layer* L, const void* x, int T, int32_t* idx, float* w, void* stream) {
   if (!L || !x || !idx || !w) return fail(K3MOE_ERR_INVALID_ARG, "NULL argument");
   if ((reinterpret_cast<uintptr_t>(x) & 15u) != 0) return fail(K3MOE_ERR_INVALID_ARG, "x must be 16-byte aligned");
+  if (!aligned_to(idx, 4) || !aligned_to(w, 4)) return fail(K3MOE_ERR_INVALID_ARG, "idx and w must be 4-byte aligned");
   if (T < 1 || T > L->dims.T_max) return fail(K3MOE_ERR_INVALID_ARG, "T=%d must be in 1..%d", T, L->dims.T_max);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   L->last_stream = s;
@@ -1142,6 +1145,8 @@ int k3moe_router_topk(k3moe_layer* L, const void* x, int T, int32_t* idx, float*
 int k3moe_bucket(k3moe_layer* L, const int32_t* idx, int T, int32_t* counts, int32_t* offsets, int32_t* perm,
                  void* stream) {
   if (!L || !idx || !counts || !offsets || !perm) return fail(K3MOE_ERR_INVALID_ARG, "NULL argument");
+  if (!aligned_to(idx, 4) || !aligned_to(counts, 4) || !aligned_to(offsets, 4) || !aligned_to(perm, 4))
+    return fail(K3MOE_ERR_INVALID_ARG, "idx, counts, offsets and perm must be 4-byte aligned");
   if (T < 1 || T > L->dims.T_max) return fail(K3MOE_ERR_INVALID_ARG, "T=%d must be in 1..%d", T, L->dims.T_max);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   L->last_stream = s;

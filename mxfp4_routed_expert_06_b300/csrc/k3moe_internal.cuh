@@ -287,4 +287,9 @@ cudaError_t launch_pack(const uint8_t* canon_nib, const uint8_t* canon_scl, int 
 // Sets the message k3moe_last_error() returns on this thread.
 void set_last_error(const char* msg);
 
+// p is a multiple of n bytes (n a power of two).  The kernels access caller buffers with their
+// natural (or vector) width and a misaligned access is a device fault, so the entry points refuse
+// such pointers before any work is queued.
+inline bool aligned_to(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; }
+
 }  // namespace k3

@@ -180,8 +180,10 @@ extern "C" int k3moe_router_topk_noalloc(const void* x_bf16, const float* W_r, c
   if (T < 1) return fail(K3MOE_ERR_INVALID_ARG, "T must be >= 1");
   if ((size_t)T * (size_t)E > kMaxLogits)
     return fail(K3MOE_ERR_INVALID_ARG, "T*E exceeds the no-alloc scratch limit of 65536 router logits");
-  if (((uintptr_t)x_bf16 & 7) != 0 || ((uintptr_t)W_r & 15) != 0)
+  if (!k3::aligned_to(x_bf16, 8) || !k3::aligned_to(W_r, 16))
     return fail(K3MOE_ERR_INVALID_ARG, "x must be 8-byte and W_r 16-byte aligned");
+  if (!k3::aligned_to(idx, 4) || !k3::aligned_to(w, 4) || (bias && !k3::aligned_to(bias, 4)))
+    return fail(K3MOE_ERR_INVALID_ARG, "idx, w and bias must be 4-byte aligned");
   unsigned char* scratch = nullptr;
   int rc = scratch_for_current_device(&scratch);
   if (rc) return rc;

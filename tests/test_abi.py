@@ -122,3 +122,22 @@ def test_pool_header_check_accepts_a_valid_header_and_names_each_mismatch():
     assert "checksum" in str(ei.value)
     with pytest.raises(k3.K3MoEError):
         k3.k3moe_pool_header_check(_header(), k3.dims(7168, 1536, 896, 16, 0))  # invalid dims
+
+
+def test_misaligned_buffers_are_refused_before_any_work():
+    """Entry points that need no layer check their pointers' alignment before touching the device
+    (these pointers are never dereferenced): a misaligned access would be a device fault."""
+    cases = [
+        # residual + RMSNorm: y float32, x / x_next / x_norm bf16
+        lambda: k3._lib.k3moe_residual_rmsnorm(0x1002, 0x2000, 1, 8, 1e-6, 0x3000, 0x4000, None),
+        lambda: k3._lib.k3moe_residual_rmsnorm(0x1000, 0x2001, 1, 8, 1e-6, 0x3000, 0x4000, None),
+        lambda: k3._lib.k3moe_residual_rmsnorm(0x1000, 0x2000, 1, 8, 1e-6, 0x3001, 0x4000, None),
+        # the no-alloc router: x 8-byte, W_r 16-byte, idx / w / bias 4-byte
+        lambda: k3._lib.k3moe_router_topk_noalloc(0x1004, 0x2000, None, 1, 8, 4, 2, 0x3000, 0x4000, None),
+        lambda: k3._lib.k3moe_router_topk_noalloc(0x1000, 0x2008, None, 1, 8, 4, 2, 0x3000, 0x4000, None),
+        lambda: k3._lib.k3moe_router_topk_noalloc(0x1000, 0x2000, None, 1, 8, 4, 2, 0x3002, 0x4000, None),
+        lambda: k3._lib.k3moe_router_topk_noalloc(0x1000, 0x2000, 0x5001, 1, 8, 4, 2, 0x3000, 0x4000, None),
+    ]
+    for i, call in enumerate(cases):
+        assert call() == k3.K3MOE_ERR_INVALID_ARG, f"case {i}"
+        assert "aligned" in k3._lib.k3moe_last_error().decode(), f"case {i}"

@@ -250,6 +250,16 @@ def test_deterministic_and_host_entry_point():
     with pytest.raises(k3.K3MoEError) as ei:
         k3.k3moe_layer_forward(L.layer, xd, 9, yd[1:1 + 9 * 512])
     assert ei.value.code == k3.K3MOE_ERR_INVALID_ARG and "y must be 16-byte aligned" in str(ei.value)
+    # int32 / float32 outputs 2 bytes off their natural alignment: refused, nothing queued
+    buf = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    p0 = buf.data_ptr()
+    h = k3._handle(L.layer)
+    assert k3._lib.k3moe_router_topk(h, xd.data_ptr(), 9, p0 + 2, p0 + 1024, None) == k3.K3MOE_ERR_INVALID_ARG
+    assert k3._lib.k3moe_router_topk(h, xd.data_ptr(), 9, p0, p0 + 1026, None) == k3.K3MOE_ERR_INVALID_ARG
+    assert k3._lib.k3moe_bucket(h, p0 + 2, 9, p0 + 1024, p0 + 2048, p0 + 3072, None) == k3.K3MOE_ERR_INVALID_ARG
+    assert k3._lib.k3moe_bucket(h, p0, 9, p0 + 1024, p0 + 2050, p0 + 3072, None) == k3.K3MOE_ERR_INVALID_ARG
+    assert "aligned" in k3._lib.k3moe_last_error().decode()
+    torch.cuda.synchronize()
     L.free()
 
 
