@@ -2,6 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl b300|reference]
                     [--workload all|decode1|decode64|prefill4096|stack4] [--tokens-per-step M]
+                    [--eager] [--no-cpu-baseline] [--experts N] [--f F] [stack4 options]
 
 Default (--workload all): one Kimi K3-shaped MoE layer (d=7168, f=1536, E=896, k=16).
   headline  decode1: single-token decode, M=1000 seeded tokens per step run back to back as
@@ -14,7 +15,14 @@ Default (--workload all): one Kimi K3-shaped MoE layer (d=7168, f=1536, E=896, k
             call per step (tensor-core grouped GEMM path).
 Every workload reports tokens/s with inputs resident, the dominant kernel's roofline from an
 event-timed pass, e2e through the host-buffer C entry point (k3moe_layer_forward_host), and the
-oracle timed on the host cores at all threads and at one thread.
+oracle timed on the host cores at all threads and at one thread.  The decode workloads' timed
+steps replay the step's layer calls as one CUDA graph captured by the library
+(k3moe_graph_create); the eager steps are timed beside them (--eager: eager only).
+
+--workload stack4: four stacked K3 layers in cache mode (pinned host pool, device slots) with
+--budget-gb, --miss-path copy-engine|zero-copy, --device-lru and --prefetch none|trace|router;
+reports the cache statistics and an LRU / Belady MIN / random replacement study of the same trace.
+--experts N and --f F give small cases with the same per-call work for profiler captures.
 
 Prints one JSON line.  With --gpus N > 1 (launched by torchrun) every rank runs an
 independent replica of the layer (the layer has no cross-GPU step on one node here);
