@@ -75,7 +75,7 @@ typedef struct {
   uint64_t hits;       /* experts found resident */
   uint64_t misses;     /* experts copied from the pinned pool */
   uint64_t evictions;  /* resident experts replaced */
-  uint64_t h2d_bytes;  /* bytes copied host -> device by misses */
+  uint64_t h2d_bytes;  /* bytes copied host -> device (misses and prefetches) */
   double h2d_ms;       /* device time of those copies (CUDA events on the copy stream) */
   uint64_t calls;      /* layer calls served */
   uint64_t prefetched; /* experts copied by k3moe_cache_prefetch (their bytes are in h2d_bytes and
@@ -141,6 +141,9 @@ int k3moe_layer_from_packed(const k3moe_dims* dims, const k3moe_pool_header* hea
  *   logit[t,e] = sum_j x[t,j]*W_r[e,j] (fp32 accumulate), sigma = 1/(1+exp(-logit)),
  *   key = sigma + bias[e]; idx[t,:] = the k experts with the largest keys in descending key
  *   order, ties to the lower expert id; w[t,i] = sigma[idx[t,i]] / sum_i sigma[idx[t,i]].
+ * From 64 tokens the logits run on the tensor cores with W_r split into bf16 hi + lo parts
+ * (each weight to 2^-18 relative), at most 4e-4 from the fp32 sum: keys closer than that may
+ * rank differently than with the CUDA-core sum used below 64 tokens.
  *   x    device pointer, [T][d] bf16, row-major, 16-byte aligned
  *   T    1..T_max
  *   idx  device pointer, [T][k] int32 (output)
@@ -190,7 +193,8 @@ int k3moe_bucket(k3moe_layer* layer, const int32_t* idx, int T, int32_t* counts,
 /* The whole layer: router -> top-k -> bucketing -> per-expert SwiGLU FFN on the MXFP4
  * weights -> combine ("four reductions", reduction 1; invariants row 5):
  *   y[t,:] = sum_{slot=0..k-1} w[t,slot] * W_d,e (silu(W_g,e x_t) * (W_u,e x_t)),
- *   e = idx[t,slot], silu(z) = z/(1+exp(-z)), summed in slot order.
+ *   e = idx[t,slot], silu(z) = z/(1+exp(-z)), summed in slot order (K3MOE_OPT_ACTIVATION
+ *   selects SiTU-GLU instead of silu).
  *   x  device pointer, [T][d] bf16 row-major, 16-byte aligned;
  *   y  device pointer, [T][d] float32 (output), 16-byte aligned.
  *   T  1..T_max.  y excludes any residual.
@@ -199,7 +203,8 @@ int k3moe_bucket(k3moe_layer* layer, const int32_t* idx, int T, int32_t* counts,
  * GEMM path (k3moe_set_option); the two agree within the accuracy bound, not bitwise.
  * In cache mode the call synchronises `stream` once (to learn which experts it needs), unless
  * every expert of the layer already sits in a slot and the cache has a slot for every expert
- * of every layer using it (then nothing can be evicted and the lookup is skipped).
+ * of every layer using it (then nothing can be evicted and the lookup is skipped), or the cache
+ * keeps its LRU state on the device (k3moe_cache_set_device_lru: no host round trip).
  * A device-resident layer's call only queues work on `stream` (no host synchronisation, no
  * allocation), so it can be captured into a CUDA graph by stream capture and replayed with the
  * same bytes, after one eager call of each path has run (that call sets the kernels' attributes);
@@ -250,10 +255,11 @@ int k3moe_sync(k3moe_layer* layer);
                                    nothing completes until the bound expires (failure-path test) */
 #define K3MOE_OPT_RING_DEPTH 5  /* value 0 (default): automatic; 1..6: stages each streaming warp
                                    keeps in flight (a tuning and test knob; results do not change) */
-#define K3MOE_OPT_TEST_FAIL_COPY 7  /* value n > 0: the n-th cache-miss copy from now reports a
-                                   failure without copying (failure-path test).  That forward returns
-                                   K3MOE_ERR_CUDA; the slot it was filling is forgotten, so later
-                                   calls copy the expert again and their results are unchanged */
+#define K3MOE_OPT_TEST_FAIL_COPY 7  /* value n > 0: the n-th cache copy from now (a miss, or a
+                                   prefetch) reports a failure without copying (failure-path test).
+                                   That call returns K3MOE_ERR_CUDA; the slot it was filling is
+                                   forgotten, so later calls copy the expert again and their
+                                   results are unchanged */
 #define K3MOE_OPT_ACTIVATION 8   /* value: K3MOE_ACT_SWIGLU (default) or K3MOE_ACT_SITU_GLU */
 #define K3MOE_OPT_MISS_PATH 9    /* cache mode: how a call's missed experts reach their slots.
                                     K3MOE_MISS_COPY_ENGINE (default): one cudaMemcpyAsync per miss
@@ -286,11 +292,12 @@ enum {
   K3MOE_K_TOPK = 1,     /* top-k for large T */
   K3MOE_K_BUCKET = 2,   /* bucketing for large T */
   K3MOE_K_GATEUP = 3,   /* gate/up + SwiGLU, register-decode path */
-  K3MOE_K_DOWN = 4,     /* down projection + combine, register-decode path */
+  K3MOE_K_DOWN = 4,     /* down projection, register-decode path */
   K3MOE_K_GEMM_GU = 5,  /* gate/up + SwiGLU, tcgen05 grouped GEMM */
   K3MOE_K_GEMM_DN = 6,  /* down projection, tcgen05 grouped GEMM */
-  K3MOE_K_COMBINE = 7,  /* slot-ordered combine for the GEMM path */
-  K3MOE_K_GATHER = 8,   /* activation gather for the GEMM path */
+  K3MOE_K_COMBINE = 7,  /* slot-ordered combine (both paths) */
+  K3MOE_K_GATHER = 8,   /* activation preparation: h -> fp16 (both paths), x gather (GEMM path),
+                           x fragments after the tensor-core router */
   K3MOE_K_COUNT = 9
 };
 typedef struct {
@@ -345,8 +352,9 @@ void k3moe_cache_destroy(k3moe_cache* cache);
  * order, takes the least recently used slot and is copied from the layer's pinned pool on the
  * cache's copy stream; this call does not wait for the copies.  A slot that a layer call still in
  * flight may read is never taken, nor one holding an expert the list names: the prefetch stops
- * at the first such slot, and `fetched` tells how far it got.  A call is known to have finished once a later call of a layer on this cache
- * has looked up its experts (that lookup waits for the stream) or after k3moe_sync.  The next
+ * at the first such slot, and `fetched` tells how far it got.  A call is known to have finished
+ * once a later call of a layer on this cache has looked up its experts (that lookup waits for the
+ * stream) or after k3moe_sync.  The next
  * layer call that uses a prefetched expert waits on its stream for the prefetch copies; its
  * output is unchanged (only which copies run, and when, differs).  Relies on the layers that
  * share a cache making their calls on one stream.  Errors: INVALID_ARG (NULL layer, a layer
@@ -399,8 +407,8 @@ int k3moe_cache_simulate(const int64_t* keys, const int64_t* call_start, int n_c
  *   x       device bf16 bits [T][d]                (read; may alias x_next or x_norm)
  *   x_next  device bf16 bits [T][d]                (written)
  *   x_norm  device bf16 bits [T][d]                (written; must not alias x_next or y)
- * Asynchronous on `stream`.  Errors: INVALID_ARG (NULL, T < 1, d < 1 or d > 65536, eps < 0
- * or not finite, x_norm aliasing x_next), CUDA.  Non-finite sums propagate. */
+ * Asynchronous on `stream`.  Errors: INVALID_ARG (NULL, misaligned, T < 1, d < 1 or d > 65536,
+ * eps < 0 or not finite, x_norm aliasing x_next), CUDA.  Non-finite sums propagate. */
 int k3moe_residual_rmsnorm(const float* y, const void* x, int T, int d, float eps, void* x_next, void* x_norm,
                            void* stream);
 
