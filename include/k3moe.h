@@ -230,7 +230,9 @@ int k3moe_layer_forward_host(k3moe_layer* layer, const void* x_bf16_host, int T,
  *   x, y    device pointers, 16-byte aligned, [calls*T][d] bf16 and [calls*T][d] float32
  *   T       1..T_max;  calls >= 1
  * The graph holds the layer's workspace: replays of graphs of one layer, and its other calls,
- * must be ordered (one stream).  Destroy it before the layer.
+ * must be ordered (one stream).  It replays the calls as captured: options set later (path,
+ * activation, wait bound) do not reach it; create a new graph for them.  Destroy it before the
+ * layer.
  * Errors: INVALID_ARG, UNSUPPORTED (cache mode), CUDA, OOM, and those of k3moe_layer_forward. */
 typedef struct k3moe_graph k3moe_graph;
 int k3moe_graph_create(k3moe_layer* layer, const void* x_bf16, int T, int calls, float* y, void* stream,
