@@ -24,6 +24,9 @@
  *          RMSNorm kernel with an epsilon (used here only as glue between stacked
  *          layers, see k3o_residual_rmsnorm).
  * Where the pages are silent the code says READING and states the reading taken.
+ * Parity unpinned: situ() (the SiTU-GLU gate, act = 1).  The pages give its ingredients and
+ * its bound but no formula, so its pins check only the properties of the reading taken.
+ * Every other function is pinned by tests/test_oracle_pins.py.
  *
  * Canonical expert layout (the input format of the library, defined by us):
  *   matrices gate W_g [f][d], up W_u [f][d], down W_d [d][f], in that order; per
